@@ -1,0 +1,546 @@
+#!/usr/bin/env python
+"""Benchmark of the csgmv LoRA path on GB300.
+
+One step = one pass of the whole path over one batch: the device batch builder
+(chunk size, stable token permutation, segments) followed by the fused
+shrink->expand kernel (csgmv_qkv).  The default workload is Llama-3-8B-shaped
+decode QKV: 256 requests x 1 token, K = 4096, q/k/v = 4096/1024/1024, c = 3,
+8 slots of rank 16.  Its inputs (13 MB) fit in L2, so steps rotate over enough
+independent input sets (own x, A, B, base and batch) that the set a step
+touches was evicted since it was last used.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead,
+on bounded token samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from segmented_gather_gemm_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "csgmv shrink+expand tokens/s at 1 GB300; % of HBM/tensor roofline vs CPU oracle"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------- workloads
+
+def make_workload(name: str, seed: int, chunk: int):
+    if name == "decode_qkv":
+        return wl.decode_qkv(seed=seed)
+    if name == "prefill_gate_up":
+        return wl.prefill_gate_up(seed=seed)
+    if name == "skewed_down_proj":
+        return wl.skewed_down_proj(seed=seed, chunk=chunk)
+    if name == "lm_head_decode":
+        return wl.lm_head_decode(seed=seed)
+    if name == "tiny":
+        return wl.tiny_single_slice(seed=seed)
+    if name == "embedding":
+        return wl.embedding_gather(seed=seed)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def token_ranks(w) -> np.ndarray:
+    """Rank of the slot of every token (request slot repeated per token)."""
+    return np.repeat(w.ranks[w.req_adapter], w.req_lens)
+
+
+def algorithmic(w, chunk: int) -> dict:
+    """Bytes and FLOPs the path must move / do for workload w: x rows of tokens
+    with a rank > 0, A rows c*r_a*K and B columns N*r_a of every used slot with
+    r_a > 0, base read + write of covered columns for those tokens, and the
+    int32 indices the kernel reads.  h costs nothing (kept on chip)."""
+    if isinstance(w, wl.EmbeddingWorkload):
+        rt = token_ranks(w)
+        s = w.s
+        nseg = sum(-(-int(n) // chunk) for n in np.bincount(np.repeat(w.req_adapter, w.req_lens)) if n)
+        b = s * 4 + s * w.R * 2 + int(rt.sum()) * 2 + 4 * (s + 2 * nseg + 1)
+        return {"bytes": b, "flops": 0, "tokens": s, "active": int((rt > 0).sum())}
+    rt = token_ranks(w)
+    act = rt > 0
+    ncov = int(w.offsets[-1] - w.offsets[0])
+    used = np.unique(np.repeat(w.req_adapter, w.req_lens)[act])
+    ra = w.ranks[used].astype(np.int64)
+    counts = np.bincount(np.repeat(w.req_adapter, w.req_lens), minlength=w.L)
+    nseg = int(sum(-(-int(n) // chunk) for n in counts if n))
+    b = (int(act.sum()) * w.K * 2 + int((w.c * ra * w.K * 2).sum()) + int((ncov * ra * 2).sum())
+         + int(act.sum()) * ncov * 4 + 4 * (w.s + 2 * nseg + 1))
+    flops = int((2 * rt.astype(np.int64) * (w.c * w.K + ncov)).sum())
+    return {"bytes": b, "flops": flops, "tokens": w.s, "active": int(act.sum())}
+
+
+def set_bytes(w) -> int:
+    if isinstance(w, wl.EmbeddingWorkload):
+        return w.ids.nbytes + w.A_emb.nbytes
+    return w.x.nbytes + w.A.nbytes + w.B.nbytes + w.base.nbytes
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("lora.cu", "device_utils.cuh", "csgmv_internal.h", "embedding.cu", "builder.cu"):
+        with open(os.path.join(ROOT, "segmented_gather_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    summary, if it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        load = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(load)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+class DeviceSet:
+    """One independent input set resident in HBM, with its own batch info."""
+
+    def __init__(self, w, chunk_override: int, max_rank: int):
+        import torch
+
+        from segmented_gather_gemm_gb300 import binding as B
+        self.w = w
+
+        def bf(b):
+            return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+
+        self.lens = torch.from_numpy(w.req_lens).cuda()
+        self.ad = torch.from_numpy(w.req_adapter).cuda()
+        self.ranks = torch.from_numpy(w.ranks).cuda()
+        if isinstance(w, wl.EmbeddingWorkload):
+            self.scal = torch.ones(w.L, dtype=torch.float32, device="cuda")
+            self.ids = torch.from_numpy(w.ids).cuda()
+            self.A = bf(w.A_emb)
+            self.out = torch.zeros((w.s, w.R), dtype=torch.bfloat16, device="cuda")
+            self.bi = B.BatchInfo.for_batch(len(w.req_lens), w.s, w.L, w.R)
+        else:
+            self.scal = torch.from_numpy(w.scalings).cuda()
+            self.x, self.A, self.B, self.y = bf(w.x), bf(w.A), bf(w.B), bf(w.base)
+            self.bi = B.BatchInfo.for_batch(w.bs, w.s, w.L, w.R, min_chunk=min(16, chunk_override or 16))
+            self.widest = int(np.max(np.diff(w.offsets)))
+        self.chunk_override = chunk_override
+
+    def build(self):
+        from segmented_gather_gemm_gb300 import binding as B
+        w = self.w
+        B.csgmv_build_batch_info(self.bi, self.lens, self.ad, w.s, self.ranks, self.scal,
+                                 max_chunk_size=w.max_chunk_size, chunk_size_override=self.chunk_override,
+                                 use_cuda_graph=True)
+
+    def compute(self):
+        from segmented_gather_gemm_gb300 import binding as B
+        w = self.w
+        if isinstance(w, wl.EmbeddingWorkload):
+            B.embedding_lora_a(self.ids, self.A, w.V, self.out, self.bi)
+        else:
+            B.csgmv_qkv(self.x, self.A, self.B, w.offsets, w.c, self.widest, self.y, self.bi)
+
+    def step(self):
+        self.build()
+        self.compute()
+
+
+def capture(torch, fn_list):
+    """One CUDA graph that runs fn_list in order on the capture stream."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for fn in fn_list:
+            fn()
+    return g
+
+
+def timed_graphs(torch, sets, n, kind, max_graph=1200):
+    """Graphs that together run exactly n steps, rotating over the sets."""
+    def fns(start, count):
+        pick = {"step": "step", "compute": "compute", "build": "build"}[kind]
+        return [getattr(sets[i % len(sets)], pick) for i in range(start, start + count)]
+    if n <= max_graph:
+        return [capture(torch, fns(0, n))]
+    g_len = max(1, max_graph // len(sets)) * len(sets)
+    full, rem = divmod(n, g_len)
+    plan = [capture(torch, fns(0, g_len))] * full
+    if rem:
+        plan.append(capture(torch, fns(full * g_len, rem)))
+    return plan
+
+
+def time_plan(torch, plan, dist=None):
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for g in plan:
+        g.replay()
+    end.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return start.elapsed_time(end) / 1e3
+
+
+def run_gpu(args):
+    import torch
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    from segmented_gather_gemm_gb300 import build as sgb
+    sgb.build()
+    from segmented_gather_gemm_gb300 import binding as B
+    B.lib()
+
+    w0 = make_workload(args.workload, 0, args.chunk)
+    per_set = set_bytes(w0)
+    nsets = args.sets or max(1, -(-2 * L2_BYTES // per_set) + 1)
+    seeds = [1000 * rank + i for i in range(nsets)]
+    ws = [w0 if s == 0 else make_workload(args.workload, s, args.chunk) for s in seeds]
+    chunk_override = args.chunk if args.workload == "skewed_down_proj" else 0
+    sets = [DeviceSet(w, chunk_override, w.R) for w in ws]
+    torch.cuda.synchronize()
+
+    # warm-up: every set once, then W steps
+    for s in sets:
+        s.step()
+    for i in range(args.warmup):
+        sets[i % nsets].step()
+    torch.cuda.synchronize()
+    status = [s.bi.device_status() for s in sets]
+    if any(status):
+        raise SystemExit(f"device status {status}")
+
+    plan = timed_graphs(torch, sets, args.steps, "step")
+    kplan = timed_graphs(torch, sets, min(args.steps, 2400) if args.steps >= nsets else nsets, "compute")
+    bplan = timed_graphs(torch, sets, min(args.steps, 2400) if args.steps >= nsets else nsets, "build")
+    time_plan(torch, plan[:1])  # graph upload / first replay
+
+    with ClockSampler(local) as clk:
+        # keep the GPU busy on the same steps for ~1 s so the clock samples
+        # describe this workload, then the timed region
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            time_plan(torch, plan[:1])
+        elapsed = time_plan(torch, plan, dist)
+    clocks = clk.summary()
+
+    k_steps = sum(1 for _ in range(args.steps))
+    k_compute = min(args.steps, 2400) if args.steps >= nsets else nsets
+    t_compute = time_plan(torch, kplan) / k_compute
+    t_build = time_plan(torch, bplan) / k_compute
+
+    if dist is not None:
+        t = torch.tensor([elapsed], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+
+    chunk = sets[0].bi.chunk_size
+    algs = [algorithmic(w, chunk) for w in ws]
+    tokens_per_step = float(np.mean([a["tokens"] for a in algs]))
+    bytes_per = float(np.mean([a["bytes"] for a in algs]))
+    flops_per = float(np.mean([a["flops"] for a in algs]))
+    value = world * k_steps * tokens_per_step / elapsed
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(torch, ws[0], chunk_override, min(args.steps, 200), world)
+
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tc = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved_gbs = bytes_per / t_compute / 1e9
+    t_hbm = bytes_per / (hbm * 1e9)
+    t_tc = flops_per / (tc * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    if bound == "hbm":
+        roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(achieved_gbs / hbm, 4)}
+    else:
+        ach = flops_per / t_compute / 1e12
+        roofline = {"bound": "tensor", "achieved": round(ach, 2), "peak": tc, "unit": "TFLOP/s",
+                    "frac": round(ach / tc, 4)}
+    tr = recorded_traffic(args.workload)
+    roofline["traffic"] = tr
+    roofline["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
+    roofline["kernel"] = "csgmv_qkv (lora_kernel fused)" if not isinstance(w0, wl.EmbeddingWorkload) \
+        else "embedding_lora_a"
+    roofline["algorithmic_bytes_per_launch"] = int(bytes_per)
+    roofline["algorithmic_flops_per_launch"] = int(flops_per)
+    roofline["kernel_us"] = round(t_compute * 1e6, 3)
+    roofline["roofline_us"] = round(max(t_hbm, t_tc) * 1e6, 3)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(elapsed / k_steps * 1e3, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w0.name, "tokens_per_step": tokens_per_step, "chunk_size": chunk,
+                   "input_sets": nsets, "set_bytes": per_set,
+                   "l2": f"rotating {nsets} input sets ({nsets * per_set / 1e6:.0f} MB > 2x L2) instead of a flush",
+                   "step": "csgmv_build_batch_info + " + ("embedding_lora_a" if isinstance(w0, wl.EmbeddingWorkload)
+                                                          else "csgmv_qkv"),
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "roofline": roofline,
+        "breakdown_us": {"build_batch_info": round(t_build * 1e6, 3), "fused": round(t_compute * 1e6, 3),
+                         "step": round(elapsed / k_steps * 1e6, 3)},
+        "gpu_launches": 2 * k_steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(ws, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(torch, w, chunk_override, steps, world):
+    """Same step through the public API with pinned HOST inputs: copy the
+    step's inputs in, build + compute, copy the result out, every step."""
+    from segmented_gather_gemm_gb300 import binding as B
+    if isinstance(w, wl.EmbeddingWorkload):
+        return None
+
+    def pin(a, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if dtype is not None:
+            t = t.view(dtype)
+        return t.pin_memory()
+
+    hx = pin(w.x.view(np.int16), torch.bfloat16)
+    hbase = pin(w.base.view(np.int16), torch.bfloat16)
+    hlens, had = pin(w.req_lens), pin(w.req_adapter)
+    hranks, hscal = pin(w.ranks), pin(w.scalings)
+    hy = torch.empty_like(hbase).pin_memory()
+    dA = torch.from_numpy(w.A.view(np.int16)).view(torch.bfloat16).cuda()
+    dB = torch.from_numpy(w.B.view(np.int16)).view(torch.bfloat16).cuda()
+    dx = torch.empty(hx.shape, dtype=torch.bfloat16, device="cuda")
+    dy = torch.empty(hbase.shape, dtype=torch.bfloat16, device="cuda")
+    dl = torch.empty_like(hlens, device="cuda")
+    da = torch.empty_like(had, device="cuda")
+    dr = torch.empty_like(hranks, device="cuda")
+    ds = torch.empty_like(hscal, device="cuda")
+    bi = B.BatchInfo.for_batch(w.bs, w.s, w.L, w.R)
+    widest = int(np.max(np.diff(w.offsets)))
+
+    def one():
+        dx.copy_(hx, non_blocking=True)
+        dy.copy_(hbase, non_blocking=True)
+        dl.copy_(hlens, non_blocking=True)
+        da.copy_(had, non_blocking=True)
+        dr.copy_(hranks, non_blocking=True)
+        ds.copy_(hscal, non_blocking=True)
+        B.csgmv_build_batch_info(bi, dl, da, w.s, dr, ds, max_chunk_size=w.max_chunk_size,
+                                 chunk_size_override=chunk_override)
+        B.csgmv_qkv(dx, dA, dB, w.offsets, w.c, widest, dy, bi)
+        hy.copy_(dy, non_blocking=True)
+
+    for _ in range(5):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    h2d = hx.nbytes + hbase.nbytes + hlens.nbytes + had.nbytes + hranks.nbytes + hscal.nbytes
+    return {"value": round(world * steps * w.s / el, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(hy.nbytes), "steps": steps,
+            "how": "wall clock over the steps (host API calls, pinned H2D + D2H copies, builder + csgmv_qkv)"}
+
+
+# --------------------------------------------------------------------------- CPU (oracle) arm
+
+def oracle_step(w, rows):
+    """The oracle on `rows` of workload w: builder over the whole batch, then the
+    fused per-token fp64 path on the sampled tokens."""
+    import oracle
+    if isinstance(w, wl.EmbeddingWorkload):
+        chunk = oracle.chunk_size(w.s, w.max_chunk_size)
+        oracle.build_batch_info(w.req_lens, w.req_adapter, chunk)
+        ta = oracle.token_adapter(w.req_lens, w.req_adapter)
+        oracle.embedding(w.ids[rows], w.A_emb, ta[rows], w.ranks)
+        return
+    chunk = w.chunk_override or oracle.chunk_size(w.s, w.max_chunk_size)
+    oracle.build_batch_info(w.req_lens, w.req_adapter, chunk)
+    ta = oracle.token_adapter(w.req_lens, w.req_adapter)
+    oracle.fused(w.x[rows], w.A, w.B, w.offsets, w.c, ta[rows], w.ranks, w.scalings, w.base[rows])
+
+
+def cpu_baseline(ws, seconds: float):
+    """The oracle as it stands on all host cores, on growing token samples of
+    the workload until about `seconds` of CPU work."""
+    import oracle
+    oracle.build()
+    w = ws[0]
+    n = 8
+    t_total, tok_total = 0.0, 0
+    i = 0
+    while t_total < seconds:
+        wi = ws[i % len(ws)]
+        rows = np.arange(min(n, wi.s))
+        t0 = time.perf_counter()
+        oracle_step(wi, rows)
+        dt = time.perf_counter() - t0
+        t_total += dt
+        tok_total += len(rows)
+        if dt < seconds / 10 and n < wi.s:
+            n = min(wi.s, n * 2)
+        i += 1
+    return {"value": round(tok_total / t_total, 2), "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{tok_total} tokens of {w.name} over {i} oracle calls "
+                      f"(full batch builder + fp64 fused per token), {t_total:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = make_workload(args.workload, 0, args.chunk)
+    # size each step's token sample so the whole run stays within ~2 minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows_n = 1
+    t0 = time.perf_counter()
+    oracle_step(w, np.arange(1))
+    per_tok = max(time.perf_counter() - t0, 1e-6)
+    rows_n = int(max(1, min(w.s, budget / per_tok)))
+    rows = np.arange(rows_n)
+    for _ in range(args.warmup):
+        oracle_step(w, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, rows)
+    el = time.perf_counter() - t0
+    value = args.steps * rows_n / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "tokens_per_step": rows_n,
+                   "step": "oracle batch builder + fp64 fused per token on a token sample"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": f"{rows_n} of {w.s} tokens per step, {args.steps} steps"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2400)
+    ap.add_argument("--warmup", type=int, default=48)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_qkv",
+                    choices=["decode_qkv", "prefill_gate_up", "skewed_down_proj", "lm_head_decode", "tiny",
+                             "embedding"])
+    ap.add_argument("--chunk", type=int, default=128, help="chunk size of skewed_down_proj")
+    ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = enough to defeat L2)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,237 @@
+// Device batch-info builder: sglang chunked_backend.py prepare_lora_batch,
+// _get_permutation (stable sort of tokens by slot) and _get_segments_info
+// (ceil(n / chunk) segments per slot run), plus _build_req_seg_indptr and the
+// CUDA-graph padding of the prepare_lora_batch use_cuda_graph branch.
+//
+// One CTA of 1024 threads does the whole batch, so the call is one launch,
+// needs no global scratch and can sit inside a CUDA graph.  The stable sort is
+// a counting sort over slots at request granularity: a request's tokens are
+// contiguous in token order and stay contiguous in sorted order, so each
+// request only needs its destination offset
+//     dest[i] = (tokens of slots < a_i) + (tokens of earlier requests on a_i).
+#include "csgmv_internal.h"
+
+namespace csgmv {
+namespace {
+
+constexpr int kBuildThreads = 1024;
+constexpr int kWarps = kBuildThreads / 32;
+
+// Exclusive block-wide scan of v; returns the prefix and writes the block
+// total to *total.  `warp_sums` is kWarps ints of shared memory.
+__device__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += n;
+    }
+    if (lane == 31) warp_sums[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += n;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    int prefix = (warp > 0 ? warp_sums[warp - 1] : 0) + inc - v;
+    *total = warp_sums[kWarps - 1];
+    __syncthreads();
+    return prefix;
+}
+
+// Largest i in [0, n) with a[i] <= key (a non-decreasing, a[0] <= key).
+__device__ int last_not_greater(const int *a, int n, int key) {
+    int lo = 0, hi = n;  // answer in [lo, hi)
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (a[mid] <= key) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kBuildThreads, 1)
+build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
+    extern __shared__ int sm[];
+    const int L = bi.max_loras;
+    int *cnt = sm;                      // [L]   tokens per slot
+    int *tokbase = cnt + L;             // [L]   first sorted position of slot a
+    int *segbase = tokbase + L;         // [L+1] first segment of slot a
+    int *run = segbase + L + 1;         // [L]   running sorted position of slot a
+    int *req_start = run + L;           // [bs+1] first token of request i
+    int *req_dest = req_start + p.bs + 1;  // [bs] first sorted position of request i
+    int *warp_sums = req_dest + p.bs;   // [32]
+    int *flags = warp_sums + kWarps;    // [0] error bits, [1] nseg
+
+    const int tid = threadIdx.x;
+    const int chunk = p.chunk;
+    if (tid == 0) { flags[0] = 0; flags[1] = 0; }
+    for (int a = tid; a < L; a += kBuildThreads) cnt[a] = 0;
+    __syncthreads();
+
+    // Slot table (lora_manager.py prepare_lora_batch: lora_ranks / scalings per slot).
+    for (int a = tid; a < L; a += kBuildThreads) {
+        int r = 0;
+        float sc = 0.f;
+        if (a < p.num_loras) {
+            r = p.ranks_in[a];
+            sc = p.scalings_in[a];
+            if (r < 0 || r > bi.max_rank) { atomicOr(&flags[0], CSGMV_STATUS_BAD_RANK); r = 0; }
+        }
+        bi.lora_ranks[a] = r;
+        bi.scalings[a] = sc;
+    }
+
+    // Per-slot token counts and validation.
+    for (int i = tid; i < p.bs; i += kBuildThreads) {
+        int a = p.req_adapter[i], l = p.req_lens[i];
+        if (a < 0 || a >= p.num_loras) atomicOr(&flags[0], CSGMV_STATUS_BAD_ADAPTER);
+        else if (l < 0) atomicOr(&flags[0], CSGMV_STATUS_BAD_LENS);
+        else atomicAdd(&cnt[a], l);
+    }
+
+    // req_start = [0, cumsum(lens)] (chunked_backend.py _build_req_seg_indptr).
+    int carry = 0;
+    for (int i0 = 0; i0 < p.bs; i0 += kBuildThreads) {
+        int i = i0 + tid;
+        int l = (i < p.bs) ? max(p.req_lens[i], 0) : 0;
+        int tot;
+        int pre = block_exclusive_scan(l, warp_sums, &tot);
+        if (i < p.bs) req_start[i] = carry + pre;
+        carry += tot;
+    }
+    if (tid == 0) {
+        req_start[p.bs] = carry;
+        if (carry != p.num_tokens) atomicOr(&flags[0], CSGMV_STATUS_BAD_LENS);
+    }
+    __syncthreads();
+
+    // Sorted-order base of each slot and its first segment.
+    int tcarry = 0, scarry = 0;
+    for (int a0 = 0; a0 < L; a0 += kBuildThreads) {
+        int a = a0 + tid;
+        int n = (a < L) ? cnt[a] : 0;
+        int ns = (n + chunk - 1) / chunk;
+        int tt, st;
+        int tpre = block_exclusive_scan(n, warp_sums, &tt);
+        int spre = block_exclusive_scan(ns, warp_sums, &st);
+        if (a < L) {
+            tokbase[a] = tcarry + tpre;
+            run[a] = tcarry + tpre;
+            segbase[a] = scarry + spre;
+        }
+        tcarry += tt;
+        scarry += st;
+    }
+    if (tid == 0) {
+        segbase[L] = scarry;
+        flags[1] = scarry;
+        if (scarry > bi.max_segments) atomicOr(&flags[0], CSGMV_STATUS_CAPACITY);
+    }
+    __syncthreads();
+
+    const int err = flags[0];
+    const int nseg = err ? 0 : flags[1];
+    if (err) {
+        if (tid == 0) {
+            *bi.num_segments_dev = 0;
+            *bi.max_len_dev = chunk;
+            bi.seg_indptr[0] = 0;
+            *bi.status = err;
+        }
+        return;
+    }
+
+    // Destination of every request: stable within a slot, so earlier requests
+    // on the same slot come first.  Warps of a 1024-request tile take turns;
+    // inside a warp, lanes with the same slot add up their predecessors' lengths.
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int i0 = 0; i0 < p.bs; i0 += kBuildThreads) {
+        int i = i0 + tid;
+        bool valid = i < p.bs;
+        int a = valid ? p.req_adapter[i] : -1;
+        int l = valid ? p.req_lens[i] : 0;
+        int pre = 0;
+        bool last = true;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            int ak = __shfl_sync(0xffffffffu, a, k);
+            int lk = __shfl_sync(0xffffffffu, l, k);
+            if (ak == a && k < lane) pre += lk;
+            if (ak == a && k > lane) last = false;
+        }
+        int nw = min(kWarps, (p.bs - i0 + 31) / 32);
+        for (int w = 0; w < nw; ++w) {
+            if (warp == w) {
+                int base = valid ? run[a] : 0;
+                __syncwarp();
+                if (valid) {
+                    req_dest[i] = base + pre;
+                    if (last) run[a] = base + pre + l;
+                }
+            }
+            __syncthreads();
+        }
+    }
+
+    // Segments (chunked_backend.py _get_segments_info): slot runs in ascending
+    // slot order, each cut into ceil(n / chunk) pieces of chunk tokens, the
+    // last one shorter.
+    if (tid == 0) bi.seg_indptr[0] = 0;
+    for (int k = tid; k < nseg; k += kBuildThreads) {
+        int a = last_not_greater(segbase, L, k);
+        int j = k - segbase[a];
+        bi.weight_indices[k] = a;
+        bi.seg_indptr[k + 1] = tokbase[a] + min((j + 1) * chunk, cnt[a]);
+    }
+    if (p.use_graph) {
+        for (int k = nseg + tid; k < bi.max_segments; k += kBuildThreads) {
+            bi.weight_indices[k] = 0;
+            bi.seg_indptr[k + 1] = p.num_tokens;
+        }
+    }
+
+    // permutation[dest of token t] = t.
+    for (int t = tid; t < p.num_tokens; t += kBuildThreads) {
+        int i = last_not_greater(req_start, p.bs + 1, t);
+        bi.permutation[req_dest[i] + (t - req_start[i])] = t;
+    }
+
+    // Per-request fields (chunked_backend.py _build_req_seg_indptr, req_weight_indices).
+    if (bi.req_seg_indptr)
+        for (int i = tid; i <= p.bs; i += kBuildThreads) bi.req_seg_indptr[i] = req_start[i];
+    if (bi.req_weight_indices)
+        for (int i = tid; i < p.bs; i += kBuildThreads) bi.req_weight_indices[i] = p.req_adapter[i];
+
+    if (tid == 0) {
+        *bi.num_segments_dev = nseg;
+        *bi.max_len_dev = chunk;
+        *bi.status = 0;
+    }
+}
+
+}  // namespace
+
+size_t build_smem_bytes(int bs, int max_loras) {
+    return sizeof(int) * ((size_t)4 * max_loras + 1 + 2 * (size_t)bs + 1 + kWarps + 2);
+}
+
+cudaError_t launch_build(const BuildParams &p, const csgmv_batch_info &bi, cudaStream_t stream) {
+    size_t smem = build_smem_bytes(p.bs, bi.max_loras);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(build_batch_info_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    build_batch_info_kernel<<<1, kBuildThreads, smem, stream>>>(p, bi);
+    return cudaGetLastError();
+}
+
+}  // namespace csgmv

@@ -1,0 +1,78 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/csgmv.h"
+
+namespace csgmv {
+
+constexpr int kMinChunkSize = 16;  // chunked_backend.py MIN_CHUNK_SIZE
+constexpr int kMaxRank = 64;       // largest buffer rank R the LoRA kernels take
+constexpr int kMaxSlices = 3;
+
+enum LoraMode { kModeFused = 0, kModeShrink = 1, kModeExpand = 2 };
+
+// Everything one launch of the shrink / expand / fused kernel needs.  Batch
+// info arrays are read on the device, so a captured graph follows whatever
+// batch was built into them last.
+struct LoraParams {
+    const uint16_t *x;   // (s, K) bf16
+    const uint16_t *A;   // (max_loras, c*R, K) bf16
+    const uint16_t *B;   // (max_loras, N, R) bf16
+    uint16_t *y;         // (s, N) bf16, in/out
+    void *h;             // (s, ldh) bf16 or f32 (shrink output / expand input)
+    int64_t K, N, ldh;
+    int h_f32;
+    int c, R;
+    int off[kMaxSlices + 1];
+    int accumulate;
+    int num_tokens;      // s, bound for permutation entries
+    int max_loras;
+    int nsplit;          // column blocks per token tile (fused / expand)
+    const int32_t *seg_indptr, *weight_indices, *permutation, *lora_ranks;
+    const float *scalings;
+    const int32_t *num_segments_dev, *max_len_dev;
+    int32_t *status;
+    // shared-memory carve-up (bytes from the dynamic base), chosen on the host
+    int sm_tok, sm_stage, sm_hpart, sm_hred, sm_hbf, sm_ex;
+    int shrink_stage_bytes, ex_stage_bytes, ex_stages;
+    int hrow_pitch;      // floats per row of hpart / hred
+    int rows_per_rank;   // TM / cluster size (reduce-scatter rows per CTA)
+    int ex_prefetch;     // 1: expand stages do not alias the shrink stages
+};
+
+struct LaunchInfo {
+    int tm;              // token tile
+    int crmax;           // compile-time bound on c*R
+    int cluster;         // CTAs per cluster (1 for expand)
+    int grid;            // CTAs
+    size_t smem;         // dynamic shared memory bytes
+};
+
+// lora.cu
+cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream,
+                        LaunchInfo *info);
+
+// builder.cu
+struct BuildParams {
+    const int32_t *req_lens, *req_adapter;
+    const int32_t *ranks_in;
+    const float *scalings_in;
+    int bs, num_tokens, num_loras, chunk, use_graph;
+};
+size_t build_smem_bytes(int bs, int max_loras);
+cudaError_t launch_build(const BuildParams &p, const csgmv_batch_info &bi, cudaStream_t stream);
+
+// embedding.cu
+struct EmbeddingParams {
+    const int32_t *ids;
+    const uint16_t *A;
+    uint16_t *out;
+    int64_t V;
+    int R;
+    int num_tokens, max_loras;
+};
+cudaError_t launch_embedding(const EmbeddingParams &p, const csgmv_batch_info &bi, cudaStream_t stream);
+
+}  // namespace csgmv
