@@ -309,7 +309,7 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         # keep the GPU busy on the same steps for ~1 s so the clock samples
         # describe this workload, then the timed region
-        t_end = time.time() + 1.0
+        t_end = time.time() + args.soak_seconds
         while time.time() < t_end:
             time_plan(torch, plan[:1])
         elapsed = time_plan(torch, plan, dist)
@@ -533,6 +533,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--soak-seconds", type=float, default=1.0,
+                    help="seconds of untimed steps before the timed region, under the clock sampler")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
