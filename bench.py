@@ -38,15 +38,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # --------------------------------------------------------------------------- workloads
 
-def make_workload(name: str, seed: int, chunk: int):
+def make_workload(name: str, seed: int, chunk: int, scale: float = 1.0, bs: int = 0):
     if name == "decode_qkv":
-        return wl.decode_qkv(seed=seed)
+        return wl.decode_qkv(seed=seed, bs=bs or 256)
     if name == "prefill_gate_up":
-        return wl.prefill_gate_up(seed=seed)
+        return wl.prefill_gate_up(seed=seed, scale_tokens=scale)
     if name == "skewed_down_proj":
-        return wl.skewed_down_proj(seed=seed, chunk=chunk)
+        return wl.skewed_down_proj(seed=seed, chunk=chunk, scale_tokens=scale)
     if name == "lm_head_decode":
-        return wl.lm_head_decode(seed=seed)
+        return wl.lm_head_decode(seed=seed, bs=bs or 512)
     if name == "tiny":
         return wl.tiny_single_slice(seed=seed)
     if name == "embedding":
@@ -282,11 +282,11 @@ def run_gpu(args):
     from segmented_gather_gemm_gb300 import binding as B
     B.lib()
 
-    w0 = make_workload(args.workload, 0, args.chunk)
+    w0 = make_workload(args.workload, 0, args.chunk, args.scale, args.bs)
     per_set = set_bytes(w0)
     nsets = args.sets or max(1, -(-2 * L2_BYTES // per_set) + 1)
     seeds = [1000 * rank + i for i in range(nsets)]
-    ws = [w0 if s == 0 else make_workload(args.workload, s, args.chunk) for s in seeds]
+    ws = [w0 if s == 0 else make_workload(args.workload, s, args.chunk, args.scale, args.bs) for s in seeds]
     chunk_override = args.chunk if args.workload == "skewed_down_proj" else 0
     sets = [DeviceSet(w, chunk_override, w.R) for w in ws]
     torch.cuda.synchronize()
@@ -490,7 +490,7 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    w = make_workload(args.workload, 0, args.chunk)
+    w = make_workload(args.workload, 0, args.chunk, args.scale, args.bs)
     # size each step's token sample so the whole run stays within ~2 minutes
     budget = 120.0 / max(1, args.steps + args.warmup)
     rows_n = 1
@@ -529,6 +529,8 @@ def main():
                     choices=["decode_qkv", "prefill_gate_up", "skewed_down_proj", "lm_head_decode", "tiny",
                              "embedding"])
     ap.add_argument("--chunk", type=int, default=128, help="chunk size of skewed_down_proj")
+    ap.add_argument("--scale", type=float, default=1.0, help="token scale of the prefill workloads")
+    ap.add_argument("--bs", type=int, default=0, help="requests of the decode workloads (0 = default)")
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = enough to defeat L2)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

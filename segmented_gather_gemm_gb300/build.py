@@ -13,7 +13,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libcsgmv.so")
-SOURCES = ["api.cu", "builder.cu", "lora.cu", "embedding.cu"]
+SOURCES = ["api.cu", "builder.cu", "embedding.cu", "lora_launch.cu", "lora_fused.cu", "lora_shrink.cu", "lora_expand.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,278 @@
+// Host side of the LoRA kernels: tile / cluster / pipeline choice, shared
+// memory carve-up, TMA descriptors, cluster launch.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "lora_tma.cuh"
+
+namespace csgmv {
+
+const void *lora_kernel_fused(int tm, int crmax);
+const void *lora_kernel_shrink(int tm, int crmax);
+const void *lora_kernel_expand(int tm, int crmax);
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_mu;
+std::map<std::pair<const void *, int>, bool> g_attr;                     // (kernel, device) attributes set
+std::map<std::tuple<const void *, int, size_t, int>, int> g_occupancy;  // (kernel, cluster, smem, dev)
+
+cudaError_t encoder() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode) return cudaSuccess;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return cudaSuccess;
+}
+
+// 2D bf16 tensor map: `inner` elements per row (contiguous), `outer` rows of
+// `row_bytes` bytes, box of box_inner x box_outer elements.
+bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+cudaError_t ensure_attrs(const void *fn, int dev, int cluster) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_pair(fn, dev);
+    if (g_attr.count(key)) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    if (cluster > 8) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    g_attr[key] = true;
+    return cudaSuccess;
+}
+
+// Co-resident clusters of `cluster` CTAs (or CTAs when cluster == 1).
+cudaError_t resident(const void *fn, int dev, int cluster, size_t smem, int *out) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_occupancy.find({fn, cluster, smem, dev});
+        if (it != g_occupancy.end()) { *out = it->second; return cudaSuccess; }
+    }
+    int n = 0;
+    cudaError_t e;
+    if (cluster > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cluster, 1, 1);
+        cfg.blockDim = dim3(kTmaThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    } else {
+        int per_sm = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kTmaThreads, smem);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        n = per_sm * sms;
+    }
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_occupancy[{fn, cluster, smem, dev}] = n;
+    *out = n;
+    return cudaSuccess;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Layout {
+    TmaKernelParams *k;
+    size_t bytes;
+};
+
+// Shared-memory carve-up for the given ring depths; returns the bytes needed.
+// The fp32 partials of the shrink alias the shrink ring: they are written
+// after the last chunk of a unit is consumed and read by the cluster before
+// any copy of the next unit lands there.
+size_t carve(TmaKernelParams &k, int mode, int tm, int cs, int S1, int S2) {
+    const int nb64 = tm >= 128 ? 1 : (tm >= 64 ? 2 : 4);
+    const int nt = 64 * nb64;
+    const int R = k.p.R;
+    const int cR = k.p.c * R;
+    size_t off = 0;
+    auto take = [&](size_t bytes, size_t align) {
+        off = align_up(off, align);
+        size_t o = off;
+        off += bytes;
+        return (int)o;
+    };
+    k.S1 = mode == kModeExpand ? 1 : S1;
+    k.S2 = mode == kModeShrink ? 1 : S2;
+    k.hp = align_up((size_t)cR, 8) + 4;
+    k.a_rows = (int)align_up((size_t)cR, 16);
+    k.o_bar = take((size_t)(2 * k.S1 + 2 * k.S2) * 8, 8);
+    k.o_run = take((size_t)(5 * k.runcap + 1 + 32) * 4, 16);
+    k.o_tok = take((size_t)tm * 4, 16);
+    if (mode != kModeExpand) {
+        k.sh_a = tm * 128;
+        k.sh_stage = (int)align_up((size_t)tm * 128 + (size_t)k.a_rows * 128, 1024);
+        const size_t ring = std::max((size_t)k.S1 * k.sh_stage, (size_t)tm * k.hp * 4);
+        k.o_sh = take(ring, 1024);
+        k.o_hpart = k.o_sh;
+        k.o_hred = cs > 1 ? take((size_t)(tm / cs) * k.hp * 4, 16) : k.o_hpart;
+    } else {
+        k.sh_a = 0;
+        k.sh_stage = 0;
+        k.o_sh = k.o_hpart = k.o_hred = 0;
+    }
+    if (mode != kModeShrink) {
+        k.ex_b = nb64 * tm * 128;
+        k.ex_stage = (int)align_up((size_t)k.ex_b + (size_t)nt * 2 * R, 1024);
+        k.o_ex = take((size_t)k.S2 * k.ex_stage, 1024);
+    } else {
+        k.ex_b = k.ex_stage = k.o_ex = 0;
+    }
+    return off + 1024;  // slack for aligning the dynamic window to 1024 bytes
+}
+
+CUtensorMapSwizzle swizzle_for_row_bytes(int bytes) {
+    return bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+         : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+         : bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
+}
+
+}  // namespace
+
+cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream,
+                        LaunchInfo *info) {
+    cudaError_t e = encoder();
+    if (e != cudaSuccess) return e;
+    const int cR = p.c * p.R;
+    const int rmax = p.R <= 16 ? 16 : (p.R <= 32 ? 32 : 64);
+    const int s = p.num_tokens;
+    const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
+    const int tps = s / slots;  // mean tokens per slot run
+    const int tm = tps <= 16 ? 16 : (tps <= 48 ? 32 : 128);
+    const void *fn = mode == kModeFused ? lora_kernel_fused(tm, rmax)
+                   : mode == kModeShrink ? lora_kernel_shrink(tm, rmax)
+                                         : lora_kernel_expand(tm, rmax);
+    if (!fn) return cudaErrorInvalidValue;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+
+    TmaKernelParams k;
+    memset(&k, 0, sizeof k);
+    k.p = p;
+    k.max_segments = bi.max_segments;
+    k.runcap = std::max(1, std::min(bi.max_segments, bi.max_loras + std::max(bi.max_bs, 1)));
+    const size_t budget = 227 * 1024;
+    const int nkc = (int)((p.K + 63) / 64);
+    const int nb64 = tm >= 128 ? 1 : (tm >= 64 ? 2 : 4);
+    const int ntile_cols = 64 * nb64;
+
+    // Cluster size: 8 unless a smaller cluster covers clearly more SMs.  Ring
+    // depths: decode tiles put every stage of a CTA in flight at once, prefill
+    // tiles get as many stages as shared memory holds (up to 8).
+    int cs_pick[3] = {0, 0, 0}, res_pick[3] = {0, 0, 0}, s1_pick[3] = {0, 0, 0}, s2_pick[3] = {0, 0, 0};
+    const int cs_list[3] = {8, 4, 2};
+    const int ncand = mode == kModeExpand ? 1 : 3;
+    int best_sms = 0;
+    for (int ci = 0; ci < ncand; ++ci) {
+        const int cs = mode == kModeExpand ? 1 : cs_list[ci];
+        if (tm % cs) continue;
+        const int kc_per = (nkc + cs - 1) / cs;
+        const int cols_per = (p.off[p.c] - p.off[0] + cs - 1) / cs;
+        const int tiles_per = std::max(1, (cols_per + ntile_cols - 1) / ntile_cols);
+        int S1 = tm <= 32 ? std::min(16, std::max(2, kc_per)) : std::min(4, std::max(2, kc_per));
+        int S2 = tm <= 32 ? std::min(8, std::max(2, tiles_per + 1)) : 8;
+        size_t smem = carve(k, mode, tm, cs, S1, S2);
+        while (smem > budget && (S1 > 2 || S2 > 2)) {
+            if (S2 > 4 || (S2 > 2 && S1 <= 2)) --S2; else --S1;
+            smem = carve(k, mode, tm, cs, S1, S2);
+        }
+        if (smem > budget) continue;
+        e = ensure_attrs(fn, dev, cs);
+        if (e != cudaSuccess) return e;
+        int res = 0;
+        if (resident(fn, dev, cs, smem, &res) != cudaSuccess) continue;
+        cs_pick[ci] = cs; res_pick[ci] = res; s1_pick[ci] = S1; s2_pick[ci] = S2;
+        best_sms = std::max(best_sms, res * cs);
+    }
+    int pick = -1;
+    for (int ci = 0; ci < ncand; ++ci)
+        if (cs_pick[ci] && res_pick[ci] * cs_pick[ci] * 100 >= best_sms * 85) { pick = ci; break; }
+    if (pick < 0) return cudaErrorInvalidConfiguration;
+    const int cs = cs_pick[pick];
+    const int best_res = res_pick[pick];
+    size_t smem = carve(k, mode, tm, cs, s1_pick[pick], s2_pick[pick]);
+
+    // Column blocks per tile when the tiles alone cannot fill the machine.
+    const int tiles_ub = (s + tm - 1) / tm + std::min(std::max(bi.bs, 1), std::max(bi.max_loras, 1));
+    if (mode == kModeShrink) {
+        k.p.nsplit = 1;
+    } else {
+        const int nblk = (p.off[p.c] - p.off[0] + 63) / 64;
+        const int max_split = std::max(1, nblk / (cs * nb64));
+        k.p.nsplit = std::max(1, std::min(best_res / std::max(tiles_ub, 1), max_split));
+    }
+    const int64_t units_ub = (int64_t)tiles_ub * k.p.nsplit;
+    const int nclusters = (int)std::max<int64_t>(1, std::min<int64_t>(best_res, units_ub));
+
+    // TMA descriptors for the weight tiles: one box per shrink chunk (all c*R
+    // rows of a slot, 64 wide) and one per expand tile (NT rows of B, all R
+    // columns).  Unused ones point at a valid tensor.
+    const int L = bi.max_loras;
+    const int nt = 64 * nb64;
+    bool ok = true;
+    if (mode != kModeExpand)
+        ok = ok && encode_2d(&k.tmA, p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2, 64, k.a_rows,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    if (mode != kModeShrink)
+        ok = ok && encode_2d(&k.tmB, p.B, (uint64_t)p.R, (uint64_t)L * p.N, (uint64_t)p.R * 2, p.R, nt,
+                             swizzle_for_row_bytes(p.R * 2));
+    if (mode == kModeExpand) k.tmA = k.tmB;
+    if (mode == kModeShrink) k.tmB = k.tmA;
+    if (!ok) return cudaErrorInvalidValue;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nclusters * cs, 1, 1);
+    cfg.blockDim = dim3(kTmaThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (info) {
+        info->tm = tm;
+        info->crmax = rmax;
+        info->cluster = cs;
+        info->grid = nclusters * cs;
+        info->smem = smem;
+    }
+    void *args[1] = {&k};
+    e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace csgmv
