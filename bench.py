@@ -100,9 +100,11 @@ def load_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("lora.cu", "device_utils.cuh", "csgmv_internal.h", "embedding.cu", "builder.cu"):
-        with open(os.path.join(ROOT, "segmented_gather_gemm_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    csrc = os.path.join(ROOT, "segmented_gather_gemm_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -264,6 +266,20 @@ def time_plan(torch, plan, dist=None):
     return start.elapsed_time(end) / 1e3
 
 
+def max_over_ranks(seconds: float, dist, device: str) -> float:
+    """The slowest rank's elapsed time (every rank gets it)."""
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, steps: int, tokens_per_step: float, elapsed: float) -> float:
+    """Tokens of all replicas / the slowest replica's time (weak scaling:
+    every rank runs its own batches)."""
+    return world * steps * tokens_per_step / elapsed
+
+
 def run_gpu(args):
     import torch
 
@@ -321,16 +337,14 @@ def run_gpu(args):
     t_build = time_plan(torch, bplan) / k_compute
 
     if dist is not None:
-        t = torch.tensor([elapsed], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+        elapsed = max_over_ranks(elapsed, dist, "cuda")
 
     chunk = sets[0].bi.chunk_size
     algs = [algorithmic(w, chunk) for w in ws]
     tokens_per_step = float(np.mean([a["tokens"] for a in algs]))
     bytes_per = float(np.mean([a["bytes"] for a in algs]))
     flops_per = float(np.mean([a["flops"] for a in algs]))
-    value = world * k_steps * tokens_per_step / elapsed
+    value = whole_job_rate(world, k_steps, tokens_per_step, elapsed)
 
     e2e = None
     if not args.no_e2e:

@@ -154,7 +154,7 @@ CSGMV_API int csgmv_build_batch_info(csgmv_batch_info *bi, const int32_t *req_le
  *   x  bf16 (s, K), s = bi->num_tokens;  A  bf16 (max_loras, c*R, K), R = bi->max_rank
  *   h  (s, ldh) of h_dtype (CSGMV_DTYPE_BF16 rounds to nearest even,
  *      CSGMV_DTYPE_F32 keeps fp32), ldh >= c*R; only columns [0, c*R) are written
- *   num_slices c in {1, 2, 3}; K a multiple of 8; R <= 64.
+ *   num_slices c in {1, 2, 3}; K a multiple of 8; R in {8, 16, 32, 64}.
  * fp32 accumulation on the tensor cores.
  */
 CSGMV_API int csgmv_shrink(const void *x, int64_t s, int64_t K, const void *A, int num_slices, void *h,

@@ -82,8 +82,9 @@ int check_offsets(const int32_t *off, int c, int64_t N, int max_slice_size) {
 int check_rank(const csgmv_batch_info *bi) {
     if (bi->max_rank > csgmv::kMaxRank)
         return fail(CSGMV_ERR_UNSUPPORTED, "max_rank %d exceeds %d", bi->max_rank, csgmv::kMaxRank);
-    if (bi->max_rank % 8 != 0)
-        return fail(CSGMV_ERR_UNSUPPORTED, "max_rank %d must be a multiple of 8 (16-byte rows of B)", bi->max_rank);
+    if (bi->max_rank != 8 && bi->max_rank != 16 && bi->max_rank != 32 && bi->max_rank != 64)
+        return fail(CSGMV_ERR_UNSUPPORTED, "max_rank %d must be 8, 16, 32 or 64 (B rows of 16..128 bytes, swizzled)",
+                    bi->max_rank);
     return CSGMV_OK;
 }
 
