@@ -11,9 +11,9 @@
 
 namespace csgmv {
 
-const void *lora_kernel_fused(int tm, int crmax);
-const void *lora_kernel_shrink(int tm, int crmax);
-const void *lora_kernel_expand(int tm, int crmax);
+const void *lora_kernel_fused(int tm, int rmax, bool tc);
+const void *lora_kernel_shrink(int tm, int rmax, bool tc);
+const void *lora_kernel_expand(int tm, int rmax, bool tc);
 
 namespace {
 
@@ -109,8 +109,8 @@ struct Layout {
 // The fp32 partials of the shrink alias the shrink ring: they are written
 // after the last chunk of a unit is consumed and read by the cluster before
 // any copy of the next unit lands there.
-size_t carve(TmaKernelParams &k, int mode, int tm, int cs, int S1, int S2) {
-    const int nb64 = tm >= 128 ? 1 : (tm >= 64 ? 2 : 4);
+size_t carve(TmaKernelParams &k, int mode, int tm, int cs, int S1, int S2, bool tc) {
+    const int nb64 = tc ? kTcCols / 64 : (tm >= 128 ? 1 : (tm >= 64 ? 2 : 4));
     const int nt = 64 * nb64;
     const int R = k.p.R;
     const int cR = k.p.c * R;
@@ -126,19 +126,25 @@ size_t carve(TmaKernelParams &k, int mode, int tm, int cs, int S1, int S2) {
     k.hp = align_up((size_t)cR, 8) + 4;
     k.a_rows = (int)align_up((size_t)cR, 16);
     k.o_bar = take((size_t)(2 * k.S1 + 2 * k.S2) * 8, 8);
+    k.o_tc = tc ? take(64, 16) : 0;
+    const size_t ah_bytes = tc ? (size_t)k.p.c * 2 * kTcAhBytes : 0;
     k.o_run = take((size_t)(5 * k.runcap + 1 + 32) * 4, 16);
     k.o_tok = take((size_t)tm * 4, 16);
     if (mode != kModeExpand) {
         k.sh_a = tm * 128;
         k.sh_stage = (int)align_up((size_t)tm * 128 + (size_t)k.a_rows * 128, 1024);
-        const size_t ring = std::max((size_t)k.S1 * k.sh_stage, (size_t)tm * k.hp * 4);
+        // the tensor-core expand's h operand tiles alias the ring as well:
+        // they are written after the reduction, when the ring is idle
+        const size_t ring = std::max({(size_t)k.S1 * k.sh_stage, (size_t)tm * k.hp * 4, ah_bytes});
         k.o_sh = take(ring, 1024);
         k.o_hpart = k.o_sh;
+        k.o_ah = k.o_sh;
         k.o_hred = cs > 1 ? take((size_t)(tm / cs) * k.hp * 4, 16) : k.o_hpart;
     } else {
         k.sh_a = 0;
         k.sh_stage = 0;
         k.o_sh = k.o_hpart = k.o_hred = 0;
+        k.o_ah = tc ? take(ah_bytes, 1024) : 0;
     }
     if (mode != kModeShrink) {
         k.ex_b = nb64 * tm * 128;
@@ -168,9 +174,13 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
     const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
     const int tps = s / slots;  // mean tokens per slot run
     const int tm = tps <= 16 ? 16 : (tps <= 48 ? 32 : 128);
-    const void *fn = mode == kModeFused ? lora_kernel_fused(tm, rmax)
-                   : mode == kModeShrink ? lora_kernel_shrink(tm, rmax)
-                                         : lora_kernel_expand(tm, rmax);
+    // Prefill tiles expand on tcgen05 when every slice edge and the B rows
+    // suit its operand layouts (16-column pieces, 32..128-byte swizzled rows).
+    bool tc = tm == 128 && mode != kModeShrink && p.R >= 16;
+    for (int j = 0; j <= p.c; ++j) tc = tc && p.off[j] % 16 == 0;
+    const void *fn = mode == kModeFused ? lora_kernel_fused(tm, rmax, tc)
+                   : mode == kModeShrink ? lora_kernel_shrink(tm, rmax, tc)
+                                         : lora_kernel_expand(tm, rmax, tc);
     if (!fn) return cudaErrorInvalidValue;
     int dev = 0;
     e = cudaGetDevice(&dev);
@@ -183,7 +193,7 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
     k.runcap = std::max(1, std::min(bi.max_segments, bi.max_loras + std::max(bi.max_bs, 1)));
     const size_t budget = 227 * 1024;
     const int nkc = (int)((p.K + 63) / 64);
-    const int nb64 = tm >= 128 ? 1 : (tm >= 64 ? 2 : 4);
+    const int nb64 = tc ? kTcCols / 64 : (tm >= 128 ? 1 : (tm >= 64 ? 2 : 4));
     const int ntile_cols = 64 * nb64;
 
     // Cluster size: 8 unless a smaller cluster covers clearly more SMs.  Ring
@@ -201,10 +211,15 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
         const int tiles_per = std::max(1, (cols_per + ntile_cols - 1) / ntile_cols);
         int S1 = tm <= 32 ? std::min(16, std::max(2, kc_per)) : std::min(4, std::max(2, kc_per));
         int S2 = tm <= 32 ? std::min(8, std::max(2, tiles_per + 1)) : 8;
-        size_t smem = carve(k, mode, tm, cs, S1, S2);
+        if (tc) {  // shrink stages that fit where the h operand tiles go anyway
+            const int sh_stage = (int)align_up((size_t)tm * 128 + align_up((size_t)cR, 16) * 128, 1024);
+            S1 = std::max(2, std::min(kc_per, (int)((size_t)p.c * 2 * kTcAhBytes / sh_stage)));
+            S2 = 4;
+        }
+        size_t smem = carve(k, mode, tm, cs, S1, S2, tc);
         while (smem > budget && (S1 > 2 || S2 > 2)) {
             if (S2 > 4 || (S2 > 2 && S1 <= 2)) --S2; else --S1;
-            smem = carve(k, mode, tm, cs, S1, S2);
+            smem = carve(k, mode, tm, cs, S1, S2, tc);
         }
         if (smem > budget) continue;
         e = ensure_attrs(fn, dev, cs);
@@ -220,7 +235,7 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
     if (pick < 0) return cudaErrorInvalidConfiguration;
     const int cs = cs_pick[pick];
     const int best_res = res_pick[pick];
-    size_t smem = carve(k, mode, tm, cs, s1_pick[pick], s2_pick[pick]);
+    size_t smem = carve(k, mode, tm, cs, s1_pick[pick], s2_pick[pick], tc);
 
     // Column blocks per tile when the tiles alone cannot fill the machine.
     const int tiles_ub = (s + tm - 1) / tm + std::min(std::max(bi.bs, 1), std::max(bi.max_loras, 1));

@@ -3,9 +3,9 @@
 
 namespace csgmv {
 
-const void *lora_kernel_shrink(int tm, int rmax) {
+const void *lora_kernel_shrink(int tm, int rmax, bool tc) {
 #define CSGMV_K(TM_, R_) \
-    if (tm == TM_ && rmax == R_) return reinterpret_cast<const void *>(lora_tma_kernel<TM_, R_, kModeShrink>);
+    if (!tc && tm == TM_ && rmax == R_) return reinterpret_cast<const void *>(lora_tma_kernel<TM_, R_, kModeShrink, false>);
     CSGMV_K(16, 16)
     CSGMV_K(16, 32)
     CSGMV_K(16, 64)

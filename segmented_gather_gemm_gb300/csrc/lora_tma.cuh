@@ -60,13 +60,21 @@ struct TmaKernelParams {
     int a_rows;          // rows of the A box (round16(c*R))
     int ex_stage, ex_b;  // expand stage bytes, B offset inside a stage
     int hp;            // floats per hpart / hred row
+    int o_tc;          // tensor-core expand: acc_full[2], acc_empty[2], TMEM base address
+    int o_ah;          // tensor-core expand: h of every slice as bf16 hi / lo operand tiles
 };
 
-template <int TM>
+// Tensor-core (tcgen05) expand: 128-token tile x 128-column stage, the fp32
+// accumulator of a stage in TMEM (two stages in flight, 256 columns).
+constexpr int kTcCols = 128;
+constexpr int kTcTmemCols = 2 * kTcCols;
+constexpr int kTcAhBytes = 128 * 128;  // one 128 x 64 bf16 operand tile (128-byte rows)
+
+template <int TM, bool TC = false>
 struct Geo {
     static constexpr int WM = TM / 16;                    // consumer warps along tokens
     static constexpr int WN = kConsumerWarps / WM;        // consumer warps along columns
-    static constexpr int NB64 = TM >= 128 ? 1 : (TM >= 64 ? 2 : 4);  // 64-column boxes per expand stage
+    static constexpr int NB64 = TC ? kTcCols / 64 : (TM >= 128 ? 1 : (TM >= 64 ? 2 : 4));  // 64-column boxes per expand stage
     static constexpr int NT = 64 * NB64;                  // expand stage width
     static constexpr int WCOLS = NT / WN;                 // columns per consumer warp
     static constexpr int EXT = WCOLS / 8;                 // n8 tiles per consumer warp
@@ -236,13 +244,185 @@ __device__ __forceinline__ void split_pair(float v0, float v1, uint32_t &hi, uin
     lo = pack_bf16x2(v0 - __bfloat162float(h0), v1 - __bfloat162float(h1));
 }
 
+// Expand of one unit on the 5th-generation tensor cores.  The tile's h (every
+// slice) goes to shared memory as bf16 hi / lo operand tiles (128-byte rows,
+// 128-byte swizzle); per 128-column stage warp 0 waits for the B tile, zeroes
+// B's padding columns [r, round16(r)) if the rank is ragged, and one lane
+// issues hi and lo tcgen05.mma per k16 step into one of two TMEM
+// accumulators (a stage that crosses a slice boundary is split there).  Every
+// warp then reads a 32-row x 32-column block of the accumulator (tcgen05.ld,
+// its TMEM lane quarter), adds base from the staged tile in fp32 and stores
+// 64-byte row pieces back through the permutation.  Warp 0 issues the next
+// stage's MMAs before its own epilogue, so the tensor core runs ahead.
+template <int TM, int MODE, typename IssueNext>
+__device__ void expand_tc(const TmaKernelParams &k, unsigned char *smem, const Unit &U, int r, float sigma, int CS,
+                          int n0, int n1, int nt, const int *tok, uint32_t tmem, uint32_t &ex_it, uint32_t &acc_it,
+                          IssueNext issue_next) {
+    static_assert(TM == 128, "the tensor-core expand takes 128-token tiles");
+    const LoraParams &p = k.p;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (nt <= 0) return;
+    Bars B = bars_of(k, smem);
+    uint64_t *acc_full = reinterpret_cast<uint64_t *>(smem + k.o_tc);
+    uint64_t *acc_empty = acc_full + 2;
+    unsigned char *ah = smem + k.o_ah;
+    const int RK = (r + 15) & ~15;
+    const int ksteps = RK / 16;
+    const int rpr = TM / CS;
+    const float *hred = reinterpret_cast<const float *>(smem + k.o_hred);
+    const int hp = k.hp;
+
+    // h of every slice: operand tile 2j (hi) and 2j+1 (lo), row m = token m of
+    // the tile, columns [0, RK) of which [r, RK) are zero.
+    const int cpr = RK / 8;
+    const int per_slice = TM * cpr;
+    for (int idx = tid; idx < p.c * per_slice; idx += kConsumerThreads) {
+        const int j = idx / per_slice, rem = idx % per_slice;
+        const int m = rem / cpr, ch = rem % cpr;
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int kk = ch * 8 + e;
+            float x = 0.f;
+            if (m < U.M && kk < r) {
+                const int col = j * r + kk;
+                if constexpr (MODE == kModeExpand) {
+                    const int t = tok[m];
+                    if (t >= 0)
+                        x = p.h_f32 ? reinterpret_cast<const float *>(p.h)[(int64_t)t * p.ldh + col]
+                                    : __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.h)[(int64_t)t * p.ldh + col]);
+                } else {
+                    const int owner = m / rpr;
+                    x = dsmem_ld_f32(dsmem_addr(hred + (m - owner * rpr) * hp + col, owner));
+                }
+            }
+            v[e] = x;
+        }
+        uint4 hi, lo;
+        split_pair(v[0], v[1], hi.x, lo.x);
+        split_pair(v[2], v[3], hi.y, lo.y);
+        split_pair(v[4], v[5], hi.z, lo.z);
+        split_pair(v[6], v[7], hi.w, lo.w);
+        const int off = m * 128 + ((ch ^ (m & 7)) << 4);
+        *reinterpret_cast<uint4 *>(ah + (2 * j) * kTcAhBytes + off) = hi;
+        *reinterpret_cast<uint4 *>(ah + (2 * j + 1) * kTcAhBytes + off) = lo;
+    }
+    fence_proxy_async_smem();  // the operand tiles are read by the tensor core
+    __syncthreads();
+
+    const uint32_t it0 = ex_it, a0 = acc_it;
+    const int Rb = p.R * 2;  // bytes per B row (32, 64 or 128: its swizzle width)
+    const int pcB = p.R / 8, shB = pc_shift_of(pcB);
+    // MMAs of stage i (whole warp 0; one lane issues)
+    auto mma_stage = [&](int i) {
+        const uint32_t g = it0 + i;
+        const int e = g % k.S2;
+        mbar_wait(&B.ex_full[e], (g / k.S2) & 1, p.status, kStatusTimeout);
+        unsigned char *bs = smem + k.o_ex + e * k.ex_stage + k.ex_b;
+        if (RK != r) {  // B columns [r, RK) are adapter padding (even NaN): zero them
+            const int c0 = r >> 3, nc = (RK >> 3) - c0;
+            for (int idx = lane; idx < kTcCols * nc; idx += 32) {
+                const int n = idx / nc, ch = c0 + idx % nc;
+                uint16_t *q16 = reinterpret_cast<uint16_t *>(bs) + swz(n, ch, pcB, shB);
+#pragma unroll
+                for (int e2 = 0; e2 < 8; ++e2)
+                    if (ch * 8 + e2 >= r) q16[e2] = 0;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+        const uint32_t ga = a0 + i;
+        const int a = ga & 1;
+        mbar_wait(&acc_empty[a], ((ga >> 1) & 1) ^ 1, p.status, kStatusTimeout);
+        tc_fence_after();
+        if (lane == 0) {
+            const int x0 = n0 + i * kTcCols;
+            const int ncols = min(n1, x0 + kTcCols) - x0;  // a multiple of 16
+            const uint32_t bsa = smem_u32(bs);
+            int c0 = 0;
+            while (c0 < ncols) {
+                const int j = slice_at(p, x0 + c0);
+                const int c1 = j + 1 < p.c ? min(ncols, p.off[j + 1] - x0) : ncols;
+                const uint32_t idesc = idesc_bf16_f32(128, c1 - c0);
+                const uint32_t d = tmem + (uint32_t)(a * kTcCols + c0);
+                const uint32_t ahi = smem_u32(ah + (2 * j) * kTcAhBytes), alo = smem_u32(ah + (2 * j + 1) * kTcAhBytes);
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    const uint64_t bd = smem_desc_kmajor(bsa + (uint32_t)(c0 * Rb + ks * 32), Rb);
+                    tc_mma_bf16(d, smem_desc_kmajor(ahi + ks * 32, 128), bd, idesc, ks > 0);
+                    tc_mma_bf16(d, smem_desc_kmajor(alo + ks * 32, 128), bd, idesc, true);
+                }
+                c0 = c1;
+            }
+            tc_commit(&acc_full[a]);
+        }
+        __syncwarp();
+    };
+
+    if (warp == 0) mma_stage(0);
+    const int quarter = warp & 3, cg = warp >> 2;  // TMEM lanes 32*quarter.., columns 32*cg..
+    for (int i = 0; i < nt; ++i) {
+        issue_next(i);
+        if (warp == 0 && i + 1 < nt) mma_stage(i + 1);
+        const uint32_t g = it0 + i;
+        const int e = g % k.S2;
+        const uint32_t ga = a0 + i;
+        const int a = ga & 1;
+        mbar_wait(&acc_full[a], (ga >> 1) & 1, p.status, kStatusTimeout);
+        mbar_wait(&B.ex_full[e], (g / k.S2) & 1, p.status, kStatusTimeout);
+        tc_fence_after();
+        __syncwarp();  // tcgen05.ld is warp-wide
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(a * kTcCols + 32 * cg), v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[a]);
+        unsigned char *ys = smem + k.o_ex + e * k.ex_stage;
+        const int x0 = n0 + i * kTcCols, x1 = min(n1, x0 + kTcCols);
+        const int row = 32 * quarter + lane;
+        if (row < U.M) {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const int lc = 32 * cg + 8 * c4;
+                if (x0 + lc < x1) {
+                    uint4 *ptr = reinterpret_cast<uint4 *>(ys + (lc >> 6) * TM * 128 + row * 128 +
+                                                           ((((lc & 63) >> 3) ^ (row & 7)) << 4));
+                    uint4 bv = p.accumulate ? *ptr : make_uint4(0, 0, 0, 0);
+                    float2 f;
+                    f = unpack_bf16x2(bv.x); bv.x = pack_bf16x2(f.x + sigma * v[8 * c4 + 0], f.y + sigma * v[8 * c4 + 1]);
+                    f = unpack_bf16x2(bv.y); bv.y = pack_bf16x2(f.x + sigma * v[8 * c4 + 2], f.y + sigma * v[8 * c4 + 3]);
+                    f = unpack_bf16x2(bv.z); bv.z = pack_bf16x2(f.x + sigma * v[8 * c4 + 4], f.y + sigma * v[8 * c4 + 5]);
+                    f = unpack_bf16x2(bv.w); bv.w = pack_bf16x2(f.x + sigma * v[8 * c4 + 6], f.y + sigma * v[8 * c4 + 7]);
+                    *ptr = bv;
+                }
+            }
+        }
+        __syncwarp();
+        // this warp's 32 rows x 32 columns, 64-byte row pieces
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int idx = lane + 32 * it, rr = idx >> 2, c4 = idx & 3;
+            const int row2 = 32 * quarter + rr, lc = 32 * cg + 8 * c4, col = x0 + lc;
+            if (row2 < U.M && col < x1) {
+                const int t = tok[row2];
+                if (t >= 0)
+                    *reinterpret_cast<uint4 *>(p.y + (int64_t)t * p.N + col) = *reinterpret_cast<const uint4 *>(
+                        ys + (lc >> 6) * TM * 128 + row2 * 128 + ((((lc & 63) >> 3) ^ (row2 & 7)) << 4));
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.ex_empty[e]);
+    }
+    ex_it += nt;
+    acc_it += nt;
+}
+
 // The sixteen warps gather the permuted x / base rows with coalesced
 // 16-byte cp.async (completion folded into the stage's mbarrier), run the
 // tensor-core math and the epilogue, and write y back with 16-byte stores.
-template <int TM, int RMAX, int MODE>
+template <int TM, int RMAX, int MODE, bool TC>
 __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int q, int CS, int nruns,
-                              int64_t nunits, int cid, int ncl) {
-    using G = Geo<TM>;
+                              int64_t nunits, int cid, int ncl, uint32_t tmem) {
+    using G = Geo<TM, TC>;
     constexpr int SHT = (3 * RMAX / 8 + G::WN - 1) / G::WN;  // shrink n8 tiles per warp (c <= 3)
     constexpr int KS = RMAX / 16;                             // expand k16 steps at most
     const LoraParams &p = k.p;
@@ -258,6 +438,7 @@ __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int
     const int kc0 = (int)((int64_t)q * nkc / CS), kc1 = (int)((int64_t)(q + 1) * nkc / CS);
     const int rpr = TM / CS;  // rows of the reduction owned by each CTA
     uint32_t sh_is = 0, sh_it = 0, ex_is = 0, ex_it = 0;
+    uint32_t acc_it = 0;  // tensor-core expand: stages whose accumulator was used
 
     for (int64_t u = cid; u < nunits; u += ncl) {
         const Unit U = decode_unit<TM>(k, smem, nruns, u);
@@ -449,7 +630,11 @@ __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int
             }
         }
 
-        if constexpr (MODE != kModeShrink) {
+        if constexpr (MODE != kModeShrink && TC) {
+            expand_tc<TM, MODE>(k, smem, U, r, sigma, CS, n0, n1, nt, tok, tmem, ex_it, acc_it, [&](int i) {
+                if (i + k.S2 - 1 < nt) issue_base(i + k.S2 - 1);
+            });
+        } else if constexpr (MODE != kModeShrink) {
             // ---------------------------------------------------------------- expand
             const int rowA = wm * 16 + (lane >> 2), rowB = rowA + 8;
             // h fragments (bf16 hi / lo pairs) of one slice for this warp's 16 rows
@@ -593,7 +778,7 @@ __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int
     }
 }
 
-template <int TM, int RMAX, int MODE>
+template <int TM, int RMAX, int MODE, bool TC>
 __global__ void __launch_bounds__(kTmaThreads, 1) lora_tma_kernel(const __grid_constant__ TmaKernelParams k) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment of the dynamic window for the 128-byte swizzle
@@ -608,19 +793,44 @@ __global__ void __launch_bounds__(kTmaThreads, 1) lora_tma_kernel(const __grid_c
         Bars B = bars_of(k, smem);
         for (int i = 0; i < k.S1; ++i) { mbar_init(&B.sh_full[i], 1 + kConsumerThreads); mbar_init(&B.sh_empty[i], kConsumerWarps); }
         for (int i = 0; i < k.S2; ++i) { mbar_init(&B.ex_full[i], 1 + kConsumerThreads); mbar_init(&B.ex_empty[i], kConsumerWarps); }
+        if constexpr (TC) {
+            uint64_t *acc = reinterpret_cast<uint64_t *>(smem + k.o_tc);
+            for (int i = 0; i < 2; ++i) { mbar_init(&acc[i], 1); mbar_init(&acc[2 + i], kConsumerWarps); }
+        }
         fence_mbar_init();
         prefetch_tmap(&k.tmA);
         prefetch_tmap(&k.tmB);
     }
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + k.o_tc + 32);
+    if constexpr (TC) {
+        if (threadIdx.x < 32) {  // one warp owns the TMEM accumulators of the CTA
+            tmem_alloc(tmem_slot, kTcTmemCols);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+    }
     int nruns = 0;
     const int ntiles = build_run_table<TM>(k, smem, &nruns);  // ends with __syncthreads
+    uint32_t tmem = 0;
+    if constexpr (TC) {
+        tc_fence_after();
+        tmem = *tmem_slot;
+    }
     const int64_t nunits = (int64_t)ntiles * k.p.nsplit;
     const int cid = blockIdx.x / CS, ncl = gridDim.x / CS;
-    consumer_loop<TM, RMAX, MODE>(k, smem, q, CS, nruns, nunits, cid, ncl);
+    consumer_loop<TM, RMAX, MODE, TC>(k, smem, q, CS, nruns, nunits, cid, ncl, tmem);
     if constexpr (MODE != kModeExpand) {
         if (CS > 1) {  // peers may still read this CTA's shared memory
             cluster_arrive();
             cluster_wait();
+        }
+    }
+    if constexpr (TC) {  // every epilogue has read its accumulator
+        tc_fence_before();
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            tc_fence_after();
+            tmem_dealloc(tmem, kTcTmemCols);
         }
     }
 }
