@@ -263,6 +263,18 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
                              swizzle_for_row_bytes(p.R * 2));
     if (mode == kModeExpand) k.tmA = k.tmB;
     if (mode == kModeShrink) k.tmB = k.tmA;
+    // row boxes of x and base for 128-token tiles of consecutive tokens
+    k.row_tma = tm == 128 ? 1 : 0;
+    if (k.row_tma && mode != kModeExpand)
+        ok = ok && encode_2d(&k.tmX, p.x, (uint64_t)p.K, (uint64_t)s, (uint64_t)p.K * 2, 64, tm,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+        k.tmX = k.tmA;
+    if (k.row_tma && mode != kModeShrink && p.accumulate)
+        ok = ok && encode_2d(&k.tmY, p.y, (uint64_t)p.N, (uint64_t)s, (uint64_t)p.N * 2, 64, tm,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+        k.tmY = k.tmA;
     if (!ok) return cudaErrorInvalidValue;
 
     cudaLaunchConfig_t cfg = {};

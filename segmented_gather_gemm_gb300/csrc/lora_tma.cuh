@@ -51,6 +51,9 @@ constexpr int kStatusTimeout = 64;                   // device status bit: a bou
 struct TmaKernelParams {
     CUtensorMap tmA;    // A (L*c*R rows, K): box 64 x round16(c*R), 128B swizzle
     CUtensorMap tmB;    // B (L*N rows, R):   box R x NT, swizzle of the R*2-byte row
+    CUtensorMap tmX;    // x (s rows, K): box 64 x TM, 128B swizzle (128-token tiles)
+    CUtensorMap tmY;    // base / y (s rows, N): box 64 x TM, 128B swizzle (128-token tiles)
+    int row_tma;        // 1: tmX / tmY are valid; tiles of consecutive tokens load rows by TMA
     LoraParams p;
     int S1, S2;        // shrink / expand ring depth
     int runcap;        // slot-run capacity of the run table
@@ -409,6 +412,7 @@ __device__ void expand_tc(const TmaKernelParams &k, unsigned char *smem, const U
                         ys + (lc >> 6) * TM * 128 + row2 * 128 + ((((lc & 63) >> 3) ^ (row2 & 7)) << 4));
             }
         }
+        fence_proxy_async_smem();  // the in-place epilogue writes before a TMA refills the stage
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.ex_empty[e]);
     }
@@ -474,6 +478,7 @@ __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int
         const float sigma = p.scalings[U.w];
         // token list of the tile (the permutation slice), shared by all warps
         int *tok = tokb;
+        fence_proxy_async_smem();  // this thread's generic writes before TMA copies reuse the memory
         __syncthreads();  // every warp is done with the previous unit's list
         for (int m = tid; m < TM; m += kConsumerThreads) {
             int t = -1;
@@ -484,6 +489,16 @@ __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int
             tok[m] = t;
         }
         __syncthreads();
+        // A tile of consecutive tokens (the usual prefill case: one request's
+        // tokens in order) loads its x and base rows as TMA boxes instead of
+        // row gathers.  Rows past the tile in the box are read, never used.
+        bool rows_tma = false;
+        if constexpr (TM == 128) {
+            bool mine = true;
+            const int t0 = tok[0];
+            for (int m = tid; m < U.M; m += kConsumerThreads) mine = mine && tok[m] == t0 + m;
+            rows_tma = __syncthreads_and(mine && t0 >= 0 && k.row_tma) != 0;
+        }
         const int cr = p.c * r;
         const int crp = (cr + 7) & ~7;
         const int ksteps = (r + 15) / 16;
@@ -500,10 +515,12 @@ __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int
             mbar_wait(&B.sh_empty[s], ((sh_is / k.S1) & 1) ^ 1, p.status, kStatusTimeout);
             __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem + k.o_sh + s * k.sh_stage);
             const int64_t k0 = (int64_t)(kc0 + ci) * 64;
-            if (tid == 0) {  // the A rows of this chunk: one TMA box
-                mbar_arrive_expect_tx(&B.sh_full[s], k.a_rows * 128);
+            if (tid == 0) {  // the A rows of this chunk: one TMA box (and the x rows: another)
+                mbar_arrive_expect_tx(&B.sh_full[s], k.a_rows * 128 + (rows_tma ? TM * 128 : 0));
                 tma_load_2d(smem + k.o_sh + s * k.sh_stage + k.sh_a, &k.tmA, (int)k0, U.w * cR, &B.sh_full[s]);
+                if (rows_tma) tma_load_2d(xs, &k.tmX, (int)k0, tok[0], &B.sh_full[s]);
             }
+            if (!rows_tma)
             for (int idx = tid; idx < U.M * 8; idx += kConsumerThreads) {
                 const int m = idx >> 3, ch = idx & 7;
                 const int t = tok[m];
@@ -520,11 +537,15 @@ __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int
             mbar_wait(&B.ex_empty[e], ((ex_is / k.S2) & 1) ^ 1, p.status, kStatusTimeout);
             unsigned char *ys = smem + k.o_ex + e * k.ex_stage;
             const int x0 = n0 + i * G::NT, x1 = min(n1, x0 + G::NT);
-            if (tid == 0) {  // the B rows of this column tile: one TMA box
-                mbar_arrive_expect_tx(&B.ex_full[e], G::NT * p.R * 2);
+            const bool base_tma = rows_tma && p.accumulate;
+            if (tid == 0) {  // the B rows of this column tile: one TMA box (base rows: NB64 more)
+                mbar_arrive_expect_tx(&B.ex_full[e], G::NT * p.R * 2 + (base_tma ? G::NB64 * TM * 128 : 0));
                 tma_load_2d(ys + k.ex_b, &k.tmB, 0, U.w * (int)p.N + x0, &B.ex_full[e]);
+                if (base_tma)
+                    for (int bx = 0; bx < G::NB64; ++bx)
+                        tma_load_2d(ys + bx * TM * 128, &k.tmY, x0 + 64 * bx, tok[0], &B.ex_full[e]);
             }
-            if (p.accumulate) {
+            if (p.accumulate && !base_tma) {
                 for (int idx = tid; idx < U.M * (G::NT / 8); idx += kConsumerThreads) {
                     const int m = idx / (G::NT / 8), c8 = idx % (G::NT / 8);
                     const int col = x0 + 8 * c8;
@@ -770,6 +791,7 @@ __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int
                     *reinterpret_cast<uint4 *>(p.y + (int64_t)t * p.N + col) =
                         *reinterpret_cast<const uint4 *>(ys + bx * TM * 128 + row * 128 + ((c8 ^ (row & 7)) << 4));
                 }
+                fence_proxy_async_smem();  // the in-place epilogue writes before a TMA refills the stage
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&B.ex_empty[e]);
                 ++ex_it;
@@ -800,6 +822,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) lora_tma_kernel(const __grid_c
         fence_mbar_init();
         prefetch_tmap(&k.tmA);
         prefetch_tmap(&k.tmB);
+        if (k.row_tma) {
+            prefetch_tmap(&k.tmX);
+            prefetch_tmap(&k.tmY);
+        }
     }
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + k.o_tc + 32);
     if constexpr (TC) {
