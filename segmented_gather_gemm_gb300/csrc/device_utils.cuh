@@ -111,7 +111,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     const uint64_t t0 = global_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > 2000000000ull) break;
+        const uint64_t dt = global_ns() - t0;
+        if (dt > 2000000000ull) break;
+        // once some wait has already given up, later ones give up after 1 ms,
+        // so a stuck launch ends in seconds rather than 2 s per wait
+        if (dt > 1000000ull && (*reinterpret_cast<volatile int32_t *>(status) & timeout_bit)) return false;
     }
     atomicOr(status, timeout_bit);
     return false;

@@ -7,13 +7,14 @@
 #include <mutex>
 #include <tuple>
 
-#include "lora_tma.cuh"
+#include "lora_ws.cuh"
 
 namespace csgmv {
 
 const void *lora_kernel_fused(int tm, int rmax, bool tc);
 const void *lora_kernel_shrink(int tm, int rmax, bool tc);
 const void *lora_kernel_expand(int tm, int rmax, bool tc);
+const void *lora_kernel_ws(int mode, int rmax);
 
 namespace {
 
@@ -63,7 +64,7 @@ cudaError_t ensure_attrs(const void *fn, int dev, int cluster) {
 }
 
 // Co-resident clusters of `cluster` CTAs (or CTAs when cluster == 1).
-cudaError_t resident(const void *fn, int dev, int cluster, size_t smem, int *out) {
+cudaError_t resident(const void *fn, int dev, int cluster, size_t smem, int *out, int threads = kTmaThreads) {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = g_occupancy.find({fn, cluster, smem, dev});
@@ -74,7 +75,7 @@ cudaError_t resident(const void *fn, int dev, int cluster, size_t smem, int *out
     if (cluster > 1) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(cluster, 1, 1);
-        cfg.blockDim = dim3(kTmaThreads, 1, 1);
+        cfg.blockDim = dim3(threads, 1, 1);
         cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -86,7 +87,7 @@ cudaError_t resident(const void *fn, int dev, int cluster, size_t smem, int *out
         e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
     } else {
         int per_sm = 0, sms = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kTmaThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         n = per_sm * sms;
     }
@@ -162,7 +163,132 @@ CUtensorMapSwizzle swizzle_for_row_bytes(int bytes) {
          : bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
 }
 
+// Shared-memory carve-up of the warp-specialized kernel.  The barriers, run
+// table and token lists come first; the rings and operand tiles start on
+// 1024-byte boundaries (128-byte swizzle).  No slack is reserved: the kernel
+// checks that its dynamic window starts on a 1024-byte boundary.
+size_t carve_ws(TmaKernelParams &k, int mode, int S1, int S2) {
+    const int R = k.p.R;
+    const int cR = k.p.c * R;
+    size_t off = 0;
+    auto take = [&](size_t bytes, size_t align) {
+        off = align_up(off, align);
+        size_t o = off;
+        off += bytes;
+        return (int)o;
+    };
+    k.S1 = mode == kModeExpand ? 1 : S1;
+    k.S2 = mode == kModeShrink ? 2 : S2;
+    k.o_bar = take((size_t)(2 * k.S1 + 3 * k.S2 + 12) * 8 + 16, 16);
+    k.o_run = take((size_t)(5 * k.runcap + 1 + 32) * 4, 16);
+    k.o_tok = take((size_t)(2 * 128 + 2) * 4, 16);
+    k.a_rows = (int)align_up((size_t)cR, 16);
+    k.o_sh = k.o_ah = k.o_ex = k.o_bring = 0;
+    k.sh_a = k.sh_stage = k.ex_b = k.ex_stage = 0;
+    if (mode != kModeExpand) {
+        k.sh_a = 128 * 128;
+        k.sh_stage = (int)align_up((size_t)k.sh_a + (size_t)k.a_rows * 128, 1024);
+        k.o_sh = take((size_t)k.S1 * k.sh_stage, 1024);
+    }
+    if (mode != kModeShrink) {
+        k.o_ah = take((size_t)k.p.c * 2 * kTcAhBytes, 1024);
+        k.o_ex = take((size_t)k.S2 * kWsBaseBytes, 1024);
+        k.o_bring = take((size_t)k.S2 * kWsCols * R * 2, 1024);
+    }
+    // at least 116 KB, so that one CTA holds an SM (and its 512 TMEM columns)
+    return std::max(off, (size_t)116 * 1024);
+}
+
 }  // namespace
+
+// 128-token tiles on the warp-specialized tcgen05 kernel (one CTA per SM).
+cudaError_t launch_lora_ws(int mode, LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream,
+                           LaunchInfo *info, int rmax) {
+    const void *fn = lora_kernel_ws(mode, rmax);
+    if (!fn) return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    TmaKernelParams k;
+    memset(&k, 0, sizeof k);
+    k.p = p;
+    k.max_segments = bi.max_segments;
+    k.runcap = std::max(1, std::min(bi.max_segments, bi.max_loras + std::max(bi.max_bs, 1)));
+    const size_t budget = 227 * 1024;
+    int S1 = 4, S2 = 8;  // S2 even: expand stages go in pairs
+    size_t smem = carve_ws(k, mode, S1, S2);
+    while (smem > budget) {
+        if (S2 > 4) S2 -= 2;
+        else if (S1 > 2) --S1;
+        else if (S2 > 2) S2 -= 2;
+        else return cudaErrorInvalidConfiguration;
+        smem = carve_ws(k, mode, S1, S2);
+    }
+    e = ensure_attrs(fn, dev, 1);
+    if (e != cudaSuccess) return e;
+    int res = 0;
+    e = resident(fn, dev, 1, smem, &res, kWsThreads);
+    if (e != cudaSuccess) return e;
+    if (res < 1) return cudaErrorInvalidConfiguration;
+
+    const int s = p.num_tokens;
+    const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
+    const int tiles_ub = (s + 127) / 128 + std::min(std::max(bi.bs, 1), std::max(bi.max_loras, 1));
+    const int tiles_est = (s + 127) / 128 + slots / 2;
+    if (mode == kModeShrink) {
+        k.p.nsplit = 1;
+    } else {
+        // column blocks per tile: about two units per CTA, each block at
+        // least 512 columns wide
+        const int nblk = (p.off[p.c] - p.off[0] + 63) / 64;
+        const int want = (2 * res + tiles_est - 1) / std::max(tiles_est, 1);
+        k.p.nsplit = std::max(1, std::min(want, std::max(1, nblk / 8)));
+    }
+    const int64_t units_ub = (int64_t)tiles_ub * k.p.nsplit;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(res, units_ub));
+
+    const int L = bi.max_loras;
+    const int cR = p.c * p.R;
+    bool ok = true;
+    if (mode != kModeShrink)
+        ok = ok && encode_2d(&k.tmB, p.B, (uint64_t)p.R, (uint64_t)L * p.N, (uint64_t)p.R * 2, p.R, kWsCols,
+                             swizzle_for_row_bytes(p.R * 2));
+    if (mode != kModeExpand) {
+        ok = ok && encode_2d(&k.tmA, p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2, 64, k.a_rows,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+        ok = ok && encode_2d(&k.tmX, p.x, (uint64_t)p.K, (uint64_t)s, (uint64_t)p.K * 2, 64, 128,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {
+        k.tmA = k.tmX = k.tmB;
+    }
+    if (mode != kModeShrink)  // base loads (when accumulating) and whole-tile stores
+        ok = ok && encode_2d(&k.tmY, p.y, (uint64_t)p.N, (uint64_t)s, (uint64_t)p.N * 2, 64, 128,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+        k.tmY = k.tmA;
+    if (mode == kModeShrink) k.tmB = k.tmA;
+    if (!ok) return cudaErrorInvalidValue;
+    k.row_tma = 1;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kWsThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    if (info) {
+        info->tm = 128;
+        info->crmax = rmax;
+        info->cluster = 1;
+        info->grid = grid;
+        info->smem = smem;
+    }
+    void *args[1] = {&k};
+    e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
 cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream,
                         LaunchInfo *info) {
@@ -178,6 +304,11 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
     // suit its operand layouts (16-column pieces, 32..128-byte swizzled rows).
     bool tc = tm == 128 && mode != kModeShrink && p.R >= 16;
     for (int j = 0; j <= p.c; ++j) tc = tc && p.off[j] % 16 == 0;
+    // Shrink-only calls on 128-token tiles of moderate K run on the
+    // warp-specialized kernel (one CTA per tile, whole K, tcgen05); the fused
+    // and expand calls measure faster on the cluster kernel.
+    if (tm == 128 && p.R >= 16 && mode == kModeShrink && p.K <= 4096)
+        return launch_lora_ws(mode, p, bi, stream, info, rmax);
     const void *fn = mode == kModeFused ? lora_kernel_fused(tm, rmax, tc)
                    : mode == kModeShrink ? lora_kernel_shrink(tm, rmax, tc)
                                          : lora_kernel_expand(tm, rmax, tc);

@@ -25,6 +25,10 @@ CASES = [
     (6, 5, 450, 128, [40, 24], 32, 2),
     (7, 64, 1, 4096, [256, 64, 64], 16, 8),
     (8, 2, 900, 72, [16], 8, 1),
+    # output columns well above K
+    (9, 3, 700, 128, [256, 128], 64, 3),
+    (10, 4, 500, 64, [128, 64, 64], 32, 3),
+    (11, 3, 400, 96, [160], 16, 2),
 ]
 
 
