@@ -154,6 +154,15 @@ template <int N>
 __device__ __forceinline__ void bulk_wait() {
     asm volatile("cp.async.bulk.wait_group %0;\n" ::"n"(N) : "memory");
 }
+// Contiguous global -> shared bulk copy completing on `bar` (16-byte aligned
+// addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
 // Arrive on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's count includes this arrival).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {

@@ -7,6 +7,7 @@
 #include <mutex>
 #include <tuple>
 
+#include "lora_small.cuh"
 #include "lora_ws.cuh"
 
 namespace csgmv {
@@ -15,6 +16,7 @@ const void *lora_kernel_fused(int tm, int rmax, bool tc);
 const void *lora_kernel_shrink(int tm, int rmax, bool tc);
 const void *lora_kernel_expand(int tm, int rmax, bool tc);
 const void *lora_kernel_ws(int mode, int rmax);
+const void *lora_kernel_small(int mode, int tm, int rmax);
 
 namespace {
 
@@ -55,10 +57,9 @@ cudaError_t ensure_attrs(const void *fn, int dev, int cluster) {
     if (g_attr.count(key)) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
-    if (cluster > 8) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-    }
+    (void)cluster;  // clusters of up to 16 CTAs
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
     g_attr[key] = true;
     return cudaSuccess;
 }
@@ -199,7 +200,143 @@ size_t carve_ws(TmaKernelParams &k, int mode, int S1, int S2) {
     return std::max(off, (size_t)116 * 1024);
 }
 
+// Shared-memory carve-up of the small-tile kernel.
+size_t carve_small(TmaKernelParams &k, int mode, int tm, int cs, int S2) {
+    const int R = k.p.R;
+    const int cR = k.p.c * R;
+    const int nkc = (int)((k.p.K + 63) / 64);
+    size_t off = 0;
+    auto take = [&](size_t bytes, size_t align) {
+        off = align_up(off, align);
+        size_t o = off;
+        off += bytes;
+        return (int)o;
+    };
+    k.S1 = 1;
+    k.S2 = mode == kModeShrink ? 1 : S2;
+    k.hp = (int)align_up((size_t)cR, 8) + 4;
+    k.a_rows = (int)align_up((size_t)cR, 16);
+    k.o_bar = take((size_t)(1 + 2 * k.S2) * 8, 8);
+    k.o_run = take((size_t)(5 * k.runcap + 1 + 32) * 4, 16);
+    k.o_tok = take((size_t)tm * 4, 16);
+    k.kc_per = 0;
+    k.xpitch = 16;
+    k.o_sh = k.o_ah = k.o_hpart = k.o_hred = 0;
+    if (mode != kModeExpand) {
+        k.kc_per = (nkc + cs - 1) / cs;
+        k.xpitch = k.kc_per * 128 + 16;  // 16 bytes of padding: conflict-free ldmatrix rows
+        k.o_sh = take((size_t)tm * k.xpitch, 16);
+        k.o_ah = take((size_t)k.kc_per * k.a_rows * 128, 1024);
+        k.o_hpart = take((size_t)tm * k.hp * 4, 16);
+        k.o_hred = cs > 1 ? take((size_t)(tm / cs) * k.hp * 4, 16) : k.o_hpart;
+    }
+    k.ypitch = 16;
+    k.ex_b = k.ex_stage = k.o_ex = 0;
+    if (mode != kModeShrink) {
+        const int nt = 256;  // columns per expand stage (Geo<16/32>::NT)
+        k.ypitch = nt * 2 + 16;
+        k.ex_b = (int)align_up((size_t)tm * k.ypitch, 1024);
+        k.ex_stage = (int)align_up((size_t)k.ex_b + (size_t)nt * R * 2, 1024);
+        k.o_ex = take((size_t)k.S2 * k.ex_stage, 1024);
+    }
+    return off + 1024;  // slack for aligning the dynamic window to 1024 bytes
+}
+
 }  // namespace
+
+// 16- and 32-token tiles (decode) on the small-tile kernel.  Returns
+// cudaErrorInvalidConfiguration when no cluster shape fits; the caller then
+// takes the streaming kernel.
+cudaError_t launch_lora_small(int mode, LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream,
+                              LaunchInfo *info, int rmax, int tm) {
+    const void *fn = lora_kernel_small(mode, tm, rmax);
+    if (!fn) return cudaErrorInvalidConfiguration;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    TmaKernelParams k;
+    memset(&k, 0, sizeof k);
+    k.p = p;
+    k.max_segments = bi.max_segments;
+    k.runcap = std::max(1, std::min(bi.max_segments, bi.max_loras + std::max(bi.max_bs, 1)));
+    const size_t budget = 227 * 1024;
+    const int s = p.num_tokens;
+    const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
+    // expected tiles: full tiles plus about half a partial tile per slot run
+    const int tiles_est = std::max(slots, s / tm + slots / 2);
+    const int ncols = p.off[p.c] - p.off[0];
+    // Cluster size: the fewest waves of units, then the largest cluster (the
+    // finest split of each unit's work).
+    const int cs_list[5] = {16, 8, 4, 2, 1};
+    int best_waves = 1 << 30, best_cs = 0, best_res = 0, best_S2 = 2;
+    for (int ci = 0; ci < 5; ++ci) {
+        const int cs = mode == kModeExpand ? 1 : cs_list[ci];
+        if (mode == kModeExpand && ci > 0) break;
+        if (tm % cs) continue;
+        const int stages = std::max(1, (ncols / cs + 255) / 256);
+        int S2 = std::min(8, std::max(2, stages + 1));
+        size_t smem = carve_small(k, mode, tm, cs, S2);
+        while (smem > budget && S2 > 2) smem = carve_small(k, mode, tm, cs, --S2);
+        if (smem > budget) continue;
+        if (ensure_attrs(fn, dev, cs) != cudaSuccess) continue;
+        int res = 0;
+        if (resident(fn, dev, cs, smem, &res) != cudaSuccess || res < 1) continue;
+        const int waves = (tiles_est + res - 1) / res;
+        if (waves < best_waves) { best_waves = waves; best_cs = cs; best_res = res; best_S2 = S2; }
+    }
+    if (best_cs == 0) return cudaErrorInvalidConfiguration;
+    const int cs = best_cs;
+    const size_t smem = carve_small(k, mode, tm, cs, best_S2);
+
+    const int tiles_ub = (s + tm - 1) / tm + std::min(std::max(bi.bs, 1), std::max(bi.max_loras, 1));
+    if (mode == kModeShrink) {
+        k.p.nsplit = 1;
+    } else {
+        const int nblk = (ncols + 63) / 64;
+        const int max_split = std::max(1, nblk / (cs * 4));
+        k.p.nsplit = std::max(1, std::min(best_res / std::max(tiles_ub, 1), max_split));
+    }
+    const int64_t units_ub = (int64_t)tiles_ub * k.p.nsplit;
+    const int nclusters = (int)std::max<int64_t>(1, std::min<int64_t>(best_res, units_ub));
+
+    const int L = bi.max_loras;
+    const int cR = p.c * p.R;
+    bool ok = true;
+    if (mode != kModeExpand)
+        ok = ok && encode_2d(&k.tmA, p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2, 64, k.a_rows,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    if (mode != kModeShrink)
+        ok = ok && encode_2d(&k.tmB, p.B, (uint64_t)p.R, (uint64_t)L * p.N, (uint64_t)p.R * 2, p.R, 256,
+                             swizzle_for_row_bytes(p.R * 2));
+    if (mode == kModeExpand) k.tmA = k.tmB;
+    if (mode == kModeShrink) k.tmB = k.tmA;
+    k.tmX = k.tmY = k.tmA;
+    if (!ok) return cudaErrorInvalidValue;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nclusters * cs, 1, 1);
+    cfg.blockDim = dim3(kConsumerThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (info) {
+        info->tm = tm;
+        info->crmax = rmax;
+        info->cluster = cs;
+        info->grid = nclusters * cs;
+        info->smem = smem;
+    }
+    void *args[1] = {&k};
+    e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
 // 128-token tiles on the warp-specialized tcgen05 kernel (one CTA per SM).
 cudaError_t launch_lora_ws(int mode, LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream,
@@ -309,6 +446,10 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
     // and expand calls measure faster on the cluster kernel.
     if (tm == 128 && p.R >= 16 && mode == kModeShrink && p.K <= 4096)
         return launch_lora_ws(mode, p, bi, stream, info, rmax);
+    if (tm <= 32) {
+        const cudaError_t es = launch_lora_small(mode, p, bi, stream, info, rmax, tm);
+        if (es != cudaErrorInvalidConfiguration) return es;
+    }
     const void *fn = mode == kModeFused ? lora_kernel_fused(tm, rmax, tc)
                    : mode == kModeShrink ? lora_kernel_shrink(tm, rmax, tc)
                                          : lora_kernel_expand(tm, rmax, tc);

@@ -66,6 +66,8 @@ struct TmaKernelParams {
     int o_tc;          // tensor-core expand: acc_full[2], acc_empty[2], TMEM base address
     int o_ah;          // tensor-core expand: h of every slice as bf16 hi / lo operand tiles
     int o_bring;       // warp-specialized kernel: B tiles of the expand stages (consecutive slots)
+    int xpitch, ypitch;  // small-tile kernel: bytes per staged x row / base row
+    int kc_per;          // small-tile kernel: 64-wide K chunks staged per CTA
 };
 
 // Tensor-core (tcgen05) expand: 128-token tile x 128-column stage, the fp32
