@@ -211,6 +211,11 @@ __device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
     asm("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr));
     return v;
 }
+__device__ __forceinline__ void dsmem_st_f4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
 // Named barrier over `count` threads (id 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");

@@ -221,14 +221,18 @@ size_t carve_small(TmaKernelParams &k, int mode, int tm, int cs, int S2) {
     k.o_tok = take((size_t)tm * 4, 16);
     k.kc_per = 0;
     k.xpitch = 16;
-    k.o_sh = k.o_ah = k.o_hpart = k.o_hred = 0;
+    k.o_sh = k.o_ah = k.o_hred = 0;
+    // h partials (shrink) and, right after them, the per-warp epilogue scratch
+    // tiles (expand): 16 rows x (256 / WN) columns each, rows padded by 16 bytes
+    const int wcols = 256 / (kConsumerWarps / (tm / 16));
+    k.o_hpart = take((size_t)tm * k.hp * 4 + (size_t)kConsumerWarps * 16 * (wcols * 2 + 16), 16);
+    k.wscr_off = (int)align_up((size_t)tm * k.hp * 4, 16);
     if (mode != kModeExpand) {
         k.kc_per = (nkc + cs - 1) / cs;
         k.xpitch = k.kc_per * 128 + 16;  // 16 bytes of padding: conflict-free ldmatrix rows
         k.o_sh = take((size_t)tm * k.xpitch, 16);
         k.o_ah = take((size_t)k.kc_per * k.a_rows * 128, 1024);
-        k.o_hpart = take((size_t)tm * k.hp * 4, 16);
-        k.o_hred = cs > 1 ? take((size_t)(tm / cs) * k.hp * 4, 16) : k.o_hpart;
+        k.o_hred = cs > 1 ? take((size_t)tm * k.hp * 4, 16) : k.o_hpart;  // every CTA's full h
     }
     k.ypitch = 16;
     k.ex_b = k.ex_stage = k.o_ex = 0;

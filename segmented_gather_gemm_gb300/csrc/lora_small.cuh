@@ -12,8 +12,9 @@
 //           one contiguous bulk copy into a padded row-major tile; mma.sync
 //           m16n8k16 with fp32 accumulators over all chunks;
 //   reduce  partials summed over the cluster through distributed shared
-//           memory (reduce-scatter; every warp then pulls h from the owner
-//           CTA as bf16 hi + lo fragment pairs);
+//           memory: each CTA sums its share of the rows and writes the sums
+//           into every CTA's copy of h, so the expand reads h locally (as
+//           bf16 hi + lo fragment pairs);
 //   expand  a ring of 256-column stages: the slot's B rows as one TMA box and
 //           each token's base row piece as one bulk copy; y = base + sigma h
 //           B^T on the tensor cores in place, then 16-byte row stores.
@@ -50,7 +51,7 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
     const SmallBars B = small_bars(k, smem);
     int *tok = reinterpret_cast<int *>(smem + k.o_tok);
     float *hpart = reinterpret_cast<float *>(smem + k.o_hpart);
-    float *hred = reinterpret_cast<float *>(smem + k.o_hred);
+    float *hfull = reinterpret_cast<float *>(smem + k.o_hred);  // [TM][hp] reduced h, every row
     unsigned char *xs = smem + k.o_sh;  // [TM][xpitch] x rows
     unsigned char *as = smem + k.o_ah;  // [kc_per][a_rows * 128] A boxes (128-byte swizzle)
     const int hp = k.hp;
@@ -171,36 +172,46 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
             // ---------------------------------------------------------------- shrink
             mbar_wait(B.x_full, x_it & 1, p.status, kStatusTimeout);
             ++x_it;
-            float acc[SHT][4];
+            // Two accumulator sets (even / odd k16 steps); per chunk every
+            // fragment is loaded before the MMAs, so the loads overlap.
+            float acc[2][SHT][4];
 #pragma unroll
-            for (int i = 0; i < SHT; ++i)
+            for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+                for (int i = 0; i < SHT; ++i)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[h2][i][e] = 0.f;
             const unsigned char *xrow = xs + (wm * 16 + (lane & 15)) * k.xpitch + 16 * (lane >> 4);
             for (int ci = 0; ci < nch; ++ci) {
                 const __nv_bfloat16 *ab = reinterpret_cast<const __nv_bfloat16 *>(as + ci * abox);
+                uint32_t a[4][4], b[4][SHT][2];
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    uint32_t a[4];
-                    ldmatrix_x4(a[0], a[1], a[2], a[3], xrow + (ci * 64 + ks * 16) * 2);
+                    ldmatrix_x4(a[ks][0], a[ks][1], a[ks][2], a[ks][3], xrow + (ci * 64 + ks * 16) * 2);
 #pragma unroll
                     for (int i = 0; i < SHT; ++i) {
                         const int j = wn + G::WN * i;
-                        if (j * 8 < crp) {
-                            uint32_t b0, b1;
-                            ldmatrix_x2(b0, b1, ab + swz(j * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1), 8, 0));
-                            mma_bf16_16816(acc[i], a, b0, b1);
-                        }
+                        if (j * 8 < crp)
+                            ldmatrix_x2(b[ks][i][0], b[ks][i][1],
+                                        ab + swz(j * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1), 8, 0));
                     }
                 }
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+                    for (int i = 0; i < SHT; ++i)
+                        if ((wn + G::WN * i) * 8 < crp) mma_bf16_16816(acc[ks & 1][i], a[ks], b[ks][i][0], b[ks][i][1]);
             }
 #pragma unroll
             for (int i = 0; i < SHT; ++i) {
                 const int j = wn + G::WN * i;
                 if (j * 8 < crp) {
+                    float v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[e] = acc[0][i][e] + acc[1][i][e];
                     const int row = wm * 16 + (lane >> 2), col = j * 8 + 2 * (lane & 3);
-                    *reinterpret_cast<float2 *>(hpart + row * hp + col) = make_float2(acc[i][0], acc[i][1]);
-                    *reinterpret_cast<float2 *>(hpart + (row + 8) * hp + col) = make_float2(acc[i][2], acc[i][3]);
+                    *reinterpret_cast<float2 *>(hpart + row * hp + col) = make_float2(v[0], v[1]);
+                    *reinterpret_cast<float2 *>(hpart + (row + 8) * hp + col) = make_float2(v[2], v[3]);
                 }
             }
             // ---------------------------------------------------------------- reduce
@@ -225,15 +236,16 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
                                 s4.x += t4[jj].x; s4.y += t4[jj].y; s4.z += t4[jj].z; s4.w += t4[jj].w;
                             }
                     }
-                    *reinterpret_cast<float4 *>(hred + rr * hp + 4 * v) = s4;
+                    for (int peer = 0; peer < CS; ++peer)
+                        dsmem_st_f4(dsmem_addr(hfull + row * hp + 4 * v, peer), s4);
                 }
-                cluster_arrive();
+                cluster_arrive();  // every CTA's hfull is complete after this barrier
                 cluster_wait();
             } else {
                 named_bar_sync(kBarConsumers, kConsumerThreads);
             }
             if constexpr (MODE == kModeShrink) {
-                const float *src = CS > 1 ? hred : hpart;
+                const float *src = CS > 1 ? hfull : hpart;
                 const int row0 = CS > 1 ? q * rpr : 0;
                 const int nrows = CS > 1 ? rpr : TM;
                 for (int idx = tid; idx < nrows * cR; idx += kConsumerThreads) {
@@ -242,7 +254,7 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
                     if (row >= U.M) continue;
                     const int t = tok[row];
                     if (t < 0) continue;
-                    const float v = col < cr ? src[rr * hp + col] : 0.f;
+                    const float v = col < cr ? src[row * hp + col] : 0.f;
                     if (p.h_f32) reinterpret_cast<float *>(p.h)[(int64_t)t * p.ldh + col] = v;
                     else reinterpret_cast<__nv_bfloat16 *>(p.h)[(int64_t)t * p.ldh + col] = __float2bfloat16_rn(v);
                 }
@@ -262,11 +274,7 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
                     if (p.h_f32) return reinterpret_cast<const float *>(p.h)[(int64_t)t * p.ldh + col];
                     return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.h)[(int64_t)t * p.ldh + col]);
                 } else {
-                    if (CS > 1) {
-                        const int owner = row / rpr;
-                        return dsmem_ld_f32(dsmem_addr(hred + (row - owner * rpr) * hp + col, owner));
-                    }
-                    return hpart[row * hp + col];
+                    return (CS > 1 ? hfull : hpart)[row * hp + col];
                 }
             };
             auto load_slice = [&](int j) {
@@ -290,6 +298,11 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
             // B tile: row n holds B[w][x0 + n][0:R], R*2 bytes, swizzled like the TMA box
             const int pcB = p.R / 8, shB = pc_shift_of(pcB);
             const bool r_ragged = p.R == 8 ? (r < 8) : (r % 16 != 0);
+            // h of the first slice this warp needs, pulled while stage 0 lands
+            if (nt > 0) {
+                const int wc = n0 + wn * G::WCOLS;
+                if (wc < min(n1, n0 + G::NT)) load_slice(slice_at(p, wc));
+            }
             for (int i = 0; i < nt; ++i) {
                 if (i + k.S2 - 1 < nt) issue_stage(i + k.S2 - 1);
                 const int e = ex_it % k.S2;
@@ -325,34 +338,44 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
                             if (x0 + lc >= x1) continue;
                             const bool use0 = jl == jh || slice_at(p, x0 + lc) == jj;
                             const bool use1 = x0 + lc + 8 < x1 && (jl == jh || slice_at(p, x0 + lc + 8) == jj);
+                            // every B fragment of the pair first, then the MMAs
+                            uint32_t bf[KS][4];
 #pragma unroll
                             for (int ks = 0; ks < KS; ++ks) {
                                 if (ks < ksteps) {
-                                    uint32_t b00, b01, b10, b11;
                                     if (RMAX == 16 && p.R == 8) {
                                         const int nrow = lc + 8 * ((lane >> 3) & 1) + (lane & 7);
-                                        ldmatrix_x2(b00, b10, bs + nrow * 8);
-                                        b01 = 0u;
-                                        b11 = 0u;
+                                        ldmatrix_x2(bf[ks][0], bf[ks][2], bs + nrow * 8);
+                                        bf[ks][1] = 0u;
+                                        bf[ks][3] = 0u;
                                     } else {
                                         const int nrow = lc + 8 * (lane >> 4) + (lane & 7);
                                         const int ch = 2 * ks + ((lane >> 3) & 1);
-                                        ldmatrix_x4(b00, b01, b10, b11, bs + swz(nrow, ch, pcB, shB));
+                                        ldmatrix_x4(bf[ks][0], bf[ks][1], bf[ks][2], bf[ks][3], bs + swz(nrow, ch, pcB, shB));
                                     }
+                                }
+                            }
+#pragma unroll
+                            for (int ks = 0; ks < KS; ++ks) {
+                                if (ks < ksteps) {
                                     if (use0) {
-                                        mma_bf16_16816(acc[t8], fhi[ks], b00, b01);
-                                        mma_bf16_16816(acc[t8], flo[ks], b00, b01);
+                                        mma_bf16_16816(acc[t8], fhi[ks], bf[ks][0], bf[ks][1]);
+                                        mma_bf16_16816(acc[t8], flo[ks], bf[ks][0], bf[ks][1]);
                                     }
                                     if (use1) {
-                                        mma_bf16_16816(acc[t8 + 1], fhi[ks], b10, b11);
-                                        mma_bf16_16816(acc[t8 + 1], flo[ks], b10, b11);
+                                        mma_bf16_16816(acc[t8 + 1], fhi[ks], bf[ks][2], bf[ks][3]);
+                                        mma_bf16_16816(acc[t8 + 1], flo[ks], bf[ks][2], bf[ks][3]);
                                     }
                                 }
                             }
                         }
                     }
                 }
-                // y = base + sigma * acc, in place in the staged base rows
+                // y = base + sigma * acc into this warp's scratch tile (the staged
+                // base rows are only read, so the next bulk copy into the stage
+                // needs no proxy fence)
+                constexpr int SP = G::WCOLS * 2 + 16;  // scratch row pitch, bytes
+                unsigned char *wsc = smem + k.o_hpart + k.wscr_off + warp * 16 * SP;
 #pragma unroll
                 for (int t8 = 0; t8 < G::EXT; ++t8) {
                     const int lc = wn * G::WCOLS + 8 * t8 + 2 * (lane & 3);
@@ -360,26 +383,26 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int row = hh ? rowB : rowA;
-                        if (row >= U.M) continue;
-                        uint32_t *ptr = reinterpret_cast<uint32_t *>(ys + row * k.ypitch + lc * 2);
-                        const float2 bv = p.accumulate ? unpack_bf16x2(*ptr) : make_float2(0.f, 0.f);
-                        *ptr = pack_bf16x2(bv.x + sigma * acc[t8][2 * hh], bv.y + sigma * acc[t8][2 * hh + 1]);
+                        const float2 bv = p.accumulate && row < U.M
+                                              ? unpack_bf16x2(*reinterpret_cast<const uint32_t *>(ys + row * k.ypitch + lc * 2))
+                                              : make_float2(0.f, 0.f);
+                        *reinterpret_cast<uint32_t *>(wsc + (row - wm * 16) * SP + (lc - wn * G::WCOLS) * 2) =
+                            pack_bf16x2(bv.x + sigma * acc[t8][2 * hh], bv.y + sigma * acc[t8][2 * hh + 1]);
                     }
                 }
                 __syncwarp();
                 // this warp's 16 rows x WCOLS columns go out as 16-byte stores
                 constexpr int CPR = G::WCOLS / 8;  // 16-byte chunks per row
                 for (int idx = lane; idx < 16 * CPR; idx += 32) {
-                    const int row = wm * 16 + idx / CPR;
-                    const int lc = wn * G::WCOLS + 8 * (idx % CPR);
-                    const int col = x0 + lc;
+                    const int rr = idx / CPR, c16 = idx % CPR;
+                    const int row = wm * 16 + rr;
+                    const int col = x0 + wn * G::WCOLS + 8 * c16;
                     if (row >= U.M || col >= x1) continue;
                     const int t = tok[row];
                     if (t < 0) continue;
                     *reinterpret_cast<uint4 *>(p.y + (int64_t)t * p.N + col) =
-                        *reinterpret_cast<const uint4 *>(ys + row * k.ypitch + lc * 2);
+                        *reinterpret_cast<const uint4 *>(wsc + rr * SP + c16 * 16);
                 }
-                fence_proxy_async_smem();  // the in-place writes before a bulk copy refills the stage
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&B.ex_empty[e]);
                 ++ex_it;

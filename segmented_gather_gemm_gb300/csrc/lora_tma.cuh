@@ -68,6 +68,7 @@ struct TmaKernelParams {
     int o_bring;       // warp-specialized kernel: B tiles of the expand stages (consecutive slots)
     int xpitch, ypitch;  // small-tile kernel: bytes per staged x row / base row
     int kc_per;          // small-tile kernel: 64-wide K chunks staged per CTA
+    int wscr_off;        // small-tile kernel: per-warp epilogue scratch, bytes after o_hpart
 };
 
 // Tensor-core (tcgen05) expand: 128-token tile x 128-column stage, the fp32
