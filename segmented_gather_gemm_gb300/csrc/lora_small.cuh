@@ -115,7 +115,8 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
                     my_bytes += abox;
                 }
         }
-        for (int m = tid; m < TM; m += kConsumerThreads) {
+        // token list, read by the last warps (the first ones are issuing TMA)
+        for (int m = kConsumerThreads - 1 - tid; m >= 0 && m < TM; m += kConsumerThreads) {
             int t = -1;
             if (m < U.M) {
                 t = p.permutation[U.p0 + m];

@@ -144,16 +144,32 @@ __device__ int build_run_table(const TmaKernelParams &k, unsigned char *smem, in
     int *run_tp = run_w + k.runcap;        // [runcap + 1]
     int *scratch = run_tp + k.runcap + 1;  // [32]
     const int tid = threadIdx.x, nt = blockDim.x;
-    int nseg = *p.num_segments_dev;
-    nseg = max(0, min(nseg, k.max_segments));
+    // Every word a thread needs is loaded in one round, bounded by the
+    // capacity rather than by the segment count (which is loaded alongside).
+    const int cap = k.max_segments;
+    const int nseg_raw = *p.num_segments_dev;
     int carry = 0;
-    for (int k0 = 0; k0 < nseg; k0 += nt) {
+    for (int k0 = 0; k0 < cap; k0 += nt) {
         const int s = k0 + tid;
-        int st = 0;
-        if (s < nseg) st = (s == 0) || (p.weight_indices[s] != p.weight_indices[s - 1]);
+        int w_here = -1, w_prev = -1, ip0 = 0, ip1 = 0;
+        if (s < cap) {
+            w_here = p.weight_indices[s];
+            if (s > 0) w_prev = p.weight_indices[s - 1];
+            ip0 = p.seg_indptr[s];
+            ip1 = p.seg_indptr[s + 1];
+        }
+        const int nseg = max(0, min(nseg_raw, cap));
+        if (k0 >= nseg) break;
+        const int st = s < nseg && (s == 0 || w_here != w_prev);
+        const int en = s < nseg && (s == nseg - 1 || p.weight_indices[min(s + 1, cap - 1)] != w_here);
         int tot;
-        int pre = block_scan(st, scratch, &tot);
-        if (st && carry + pre < k.runcap) run_seg[carry + pre] = s;
+        const int pre = block_scan(st, scratch, &tot);
+        const int run = carry + pre + st - 1;  // run of segment s
+        if (st && run < k.runcap) {
+            run_w[run] = w_here;
+            run_p0[run] = max(0, min(ip0, p.num_tokens));
+        }
+        if (en && run >= 0 && run < k.runcap) run_len[run] = max(0, min(ip1, p.num_tokens));  // run end for now
         carry += tot;
     }
     int nruns = carry;
@@ -167,17 +183,12 @@ __device__ int build_run_table(const TmaKernelParams &k, unsigned char *smem, in
         const int r = r0 + tid;
         int tiles = 0;
         if (r < nruns) {
-            const int s0 = run_seg[r];
-            const int s1 = r + 1 < nruns ? run_seg[r + 1] : nseg;
-            int a = max(0, min(p.seg_indptr[s0], p.num_tokens));
-            int b = max(a, min(p.seg_indptr[s1], p.num_tokens));
-            run_p0[r] = a;
-            run_len[r] = b - a;
-            run_w[r] = p.weight_indices[s0];
-            tiles = (b - a + TM - 1) / TM;
+            const int len = max(0, run_len[r] - run_p0[r]);
+            run_len[r] = len;
+            tiles = (len + TM - 1) / TM;
         }
         int tot;
-        int pre = block_scan(tiles, scratch, &tot);
+        const int pre = block_scan(tiles, scratch, &tot);
         if (r < nruns) run_tp[r] = tcarry + pre;
         tcarry += tot;
     }
