@@ -99,10 +99,12 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources of the shrink / expand / fused kernels and their
+    launcher (the kernels a recorded traffic figure belongs to)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "segmented_gather_gemm_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
+        if f.startswith("lora_") or f in ("device_utils.cuh", "csgmv_internal.h"):
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(fh.read())
     return h.hexdigest()[:16]
@@ -367,7 +369,7 @@ def run_gpu(args):
     tr = recorded_traffic(args.workload)
     roofline["traffic"] = tr
     roofline["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
-    roofline["kernel"] = "csgmv_qkv (lora_kernel fused)" if not isinstance(w0, wl.EmbeddingWorkload) \
+    roofline["kernel"] = "csgmv_qkv (fused shrink->expand)" if not isinstance(w0, wl.EmbeddingWorkload) \
         else "embedding_lora_a"
     roofline["algorithmic_bytes_per_launch"] = int(bytes_per)
     roofline["algorithmic_flops_per_launch"] = int(flops_per)
