@@ -148,9 +148,12 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
     }
 
     // Destination of every request: stable within a slot, so earlier requests
-    // on the same slot come first.  Warps of a 1024-request tile take turns;
-    // inside a warp, lanes with the same slot add up their predecessors' lengths.
+    // on the same slot come first.  Per 1024-request tile: lanes of a warp
+    // with the same slot add up their predecessors' lengths, the last such
+    // lane posts the warp's total for the slot, and one thread per slot turns
+    // the warp totals into running offsets (three barriers per tile).
     const int lane = tid & 31, warp = tid >> 5;
+    int *wsum = flags + 2;  // [kWarps][L]
     for (int i0 = 0; i0 < p.bs; i0 += kBuildThreads) {
         int i = i0 + tid;
         bool valid = i < p.bs;
@@ -165,18 +168,22 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
             if (ak == a && k < lane) pre += lk;
             if (ak == a && k > lane) last = false;
         }
-        int nw = min(kWarps, (p.bs - i0 + 31) / 32);
-        for (int w = 0; w < nw; ++w) {
-            if (warp == w) {
-                int base = valid ? run[a] : 0;
-                __syncwarp();
-                if (valid) {
-                    req_dest[i] = base + pre;
-                    if (last) run[a] = base + pre + l;
-                }
+        for (int x = tid; x < kWarps * L; x += kBuildThreads) wsum[x] = 0;
+        __syncthreads();
+        if (valid && last) wsum[warp * L + a] = pre + l;
+        __syncthreads();
+        for (int b = tid; b < L; b += kBuildThreads) {
+            int running = run[b];
+            for (int w = 0; w < kWarps; ++w) {
+                const int v = wsum[w * L + b];
+                wsum[w * L + b] = running;
+                running += v;
             }
-            __syncthreads();
+            run[b] = running;
         }
+        __syncthreads();
+        if (valid) req_dest[i] = wsum[warp * L + a] + pre;
+        __syncthreads();  // wsum is reused by the next tile
     }
 
     // Segments (chunked_backend.py _get_segments_info): slot runs in ascending
@@ -218,7 +225,7 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
 }  // namespace
 
 size_t build_smem_bytes(int bs, int max_loras) {
-    return sizeof(int) * ((size_t)4 * max_loras + 1 + 2 * (size_t)bs + 1 + kWarps + 2);
+    return sizeof(int) * ((size_t)4 * max_loras + 1 + 2 * (size_t)bs + 1 + kWarps + 2 + (size_t)kWarps * max_loras);
 }
 
 cudaError_t launch_build(const BuildParams &p, const csgmv_batch_info &bi, cudaStream_t stream) {
