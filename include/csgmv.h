@@ -180,18 +180,29 @@ CSGMV_API int csgmv_expand(const void *h, int h_dtype, int64_t ldh, const void *
                  int accumulate, const csgmv_batch_info *bi, csgmv_stream_t stream);
 
 /*
- * Fused shrink -> expand with h kept on chip (chunked_backend.py run_qkv_lora
- * and run_gate_up_lora; c = 1 is the single-projection pair
- * run_lora_a_sgemm + run_lora_b_sgemm):
+ * Fused shrink -> expand (chunked_backend.py run_qkv_lora and
+ * run_gate_up_lora; c = 1 is the single-projection pair run_lora_a_sgemm +
+ * run_lora_b_sgemm):
  *     base_output[t][n] += sigma_w * sum_k (sum_i x[t][i] A[w][j*r+k][i]) B[w][n][k]
- * for n in slice j = [off[j], off[j+1]).  h stays fp32 (reduced across a
- * thread-block cluster in distributed shared memory), so the only rounding
+ * for n in slice j = [off[j], off[j+1]).  h stays fp32, so the only rounding
  * to bf16 is the final store.  Shapes and limits as csgmv_shrink and
  * csgmv_expand; base_output is bf16 (s, N), updated in place.
+ *   workspace, workspace_bytes   optional device scratch for h (NULL / 0 for
+ *       none).  Without it h never leaves the chip (reduced across a
+ *       thread-block cluster in distributed shared memory).  With at least
+ *       csgmv_qkv_workspace_bytes() bytes, batches of long per-slot runs and
+ *       K <= 4096 (prefill) may instead run the shrink and the expand as two
+ *       kernels with fp32 h in the workspace, which is faster there.  Its
+ *       contents on entry do not matter; on return they are unspecified.  It
+ *       must be 16-byte aligned and must not overlap any other argument.
  */
 CSGMV_API int csgmv_qkv(const void *x, int64_t K, const void *A, const void *B, int64_t N,
               const int32_t *slice_offsets, int num_slices, int max_slice_size, void *base_output,
-              const csgmv_batch_info *bi, csgmv_stream_t stream);
+              void *workspace, size_t workspace_bytes, const csgmv_batch_info *bi, csgmv_stream_t stream);
+
+/* Workspace bytes that let csgmv_qkv use its two-kernel path for any batch
+ * of this batch info: max_tokens * num_slices * max_rank * 4 (fp32 h). */
+CSGMV_API size_t csgmv_qkv_workspace_bytes(const csgmv_batch_info *bi, int num_slices);
 
 /*
  * Embedding LoRA-A gather (base_backend.py run_lora_a_embedding;

@@ -22,7 +22,8 @@ STATUS_BITS = {
 }
 
 EXPORTED = ["csgmv_last_error", "csgmv_version", "csgmv_chunk_size", "csgmv_batch_info_capacity",
-            "csgmv_build_batch_info", "csgmv_shrink", "csgmv_expand", "csgmv_qkv", "embedding_lora_a"]
+            "csgmv_build_batch_info", "csgmv_shrink", "csgmv_expand", "csgmv_qkv", "csgmv_qkv_workspace_bytes",
+            "embedding_lora_a"]
 
 
 class CsgmvError(RuntimeError):
@@ -63,7 +64,8 @@ def lib():
         "csgmv_build_batch_info": (i32, [bip, vp, vp, i32, i32, vp, vp, i32, i32, i32, i32, vp]),
         "csgmv_shrink": (i32, [vp, i64, i64, vp, i32, vp, i32, i64, bip, vp]),
         "csgmv_expand": (i32, [vp, i32, i64, vp, i64, i32p, i32, i32, vp, i32, bip, vp]),
-        "csgmv_qkv": (i32, [vp, i64, vp, vp, i64, i32p, i32, i32, vp, bip, vp]),
+        "csgmv_qkv": (i32, [vp, i64, vp, vp, i64, i32p, i32, i32, vp, vp, ctypes.c_size_t, bip, vp]),
+        "csgmv_qkv_workspace_bytes": (ctypes.c_size_t, [bip, i32]),
         "embedding_lora_a": (i32, [vp, vp, i64, i32, vp, bip, vp]),
     }
     for name, (res, args) in sig.items():
@@ -194,12 +196,19 @@ def csgmv_expand(h: torch.Tensor, B: torch.Tensor, slice_offsets, num_slices: in
 
 
 def csgmv_qkv(x: torch.Tensor, A: torch.Tensor, B: torch.Tensor, slice_offsets, num_slices: int,
-              max_slice_size: int, base_output: torch.Tensor, bi: BatchInfo, stream=None) -> torch.Tensor:
+              max_slice_size: int, base_output: torch.Tensor, bi: BatchInfo, stream=None,
+              workspace: torch.Tensor | None = None) -> torch.Tensor:
     K = int(x.shape[1])
     N = int(base_output.shape[1])
+    ws = _ptr(workspace) if workspace is not None else None
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().csgmv_qkv(_ptr(x), K, _ptr(A), _ptr(B), N, _offsets(slice_offsets), int(num_slices),
-                           int(max_slice_size), _ptr(base_output), ctypes.byref(bi.c), _stream(stream)))
+                           int(max_slice_size), _ptr(base_output), ws, wsb, ctypes.byref(bi.c), _stream(stream)))
     return base_output
+
+
+def csgmv_qkv_workspace_bytes(bi: BatchInfo, num_slices: int) -> int:
+    return int(lib().csgmv_qkv_workspace_bytes(ctypes.byref(bi.c), int(num_slices)))
 
 
 def embedding_lora_a(input_ids: torch.Tensor, A_emb: torch.Tensor, vocab_size: int, out: torch.Tensor,

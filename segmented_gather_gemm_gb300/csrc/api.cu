@@ -232,9 +232,14 @@ int csgmv_expand(const void *h, int h_dtype, int64_t ldh, const void *B, int64_t
     return CSGMV_OK;
 }
 
+size_t csgmv_qkv_workspace_bytes(const csgmv_batch_info *bi, int num_slices) {
+    if (!bi || bi->max_tokens < 0 || bi->max_rank < 0 || num_slices < 1 || num_slices > csgmv::kMaxSlices) return 0;
+    return (size_t)bi->max_tokens * num_slices * bi->max_rank * 4;
+}
+
 int csgmv_qkv(const void *x, int64_t K, const void *A, const void *B, int64_t N, const int32_t *slice_offsets,
-              int num_slices, int max_slice_size, void *base_output, const csgmv_batch_info *bi,
-              csgmv_stream_t stream) {
+              int num_slices, int max_slice_size, void *base_output, void *workspace, size_t workspace_bytes,
+              const csgmv_batch_info *bi, csgmv_stream_t stream) {
     int rc = check_bi(bi, true);
     if (rc) return rc;
     if ((rc = check_rank(bi))) return rc;
@@ -259,6 +264,34 @@ int csgmv_qkv(const void *x, int64_t K, const void *A, const void *B, int64_t N,
     p.c = num_slices;
     for (int j = 0; j <= num_slices; ++j) p.off[j] = slice_offsets[j];
     p.accumulate = 1;
+    const size_t hbytes = (size_t)s * num_slices * bi->max_rank * 4;
+    if (workspace && workspace_bytes >= hbytes && csgmv::qkv_split_pays(p, *bi)) {
+        if (!aligned16(workspace)) return fail(CSGMV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+        if (overlaps_batch_info(bi, workspace, hbytes) ||
+            overlaps(workspace, hbytes, base_output, (size_t)s * N * 2))
+            return fail(CSGMV_ERR_INVALID_ARG, "workspace overlaps the batch info or base_output");
+        // shrink into the workspace (fp32 h, columns [0, c*R)), then expand onto base_output
+        csgmv::LoraParams ps = p;
+        ps.B = nullptr;
+        ps.y = nullptr;
+        ps.N = 0;
+        ps.h = workspace;
+        ps.h_f32 = 1;
+        ps.ldh = (int64_t)num_slices * bi->max_rank;
+        ps.accumulate = 0;
+        cudaError_t e = csgmv::launch_lora(csgmv::kModeShrink, ps, *bi, reinterpret_cast<cudaStream_t>(stream), nullptr);
+        if (e != cudaSuccess) return cuda_fail(e, "csgmv_qkv shrink launch");
+        csgmv::LoraParams pe = p;
+        pe.x = nullptr;
+        pe.A = nullptr;
+        pe.K = 0;
+        pe.h = workspace;
+        pe.h_f32 = 1;
+        pe.ldh = ps.ldh;
+        e = csgmv::launch_lora(csgmv::kModeExpand, pe, *bi, reinterpret_cast<cudaStream_t>(stream), nullptr);
+        if (e != cudaSuccess) return cuda_fail(e, "csgmv_qkv expand launch");
+        return CSGMV_OK;
+    }
     cudaError_t e = csgmv::launch_lora(csgmv::kModeFused, p, *bi, reinterpret_cast<cudaStream_t>(stream), nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "csgmv_qkv launch");
     return CSGMV_OK;

@@ -53,6 +53,8 @@ struct LaunchInfo {
 // lora.cu
 cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream,
                         LaunchInfo *info);
+// Whether csgmv_qkv should run as shrink + expand through a workspace.
+bool qkv_split_pays(const LoraParams &p, const csgmv_batch_info &bi);
 
 // builder.cu
 struct BuildParams {

@@ -431,6 +431,23 @@ cudaError_t launch_lora_ws(int mode, LoraParams &p, const csgmv_batch_info &bi, 
     return cudaGetLastError();
 }
 
+// Token tile for a batch: 16 for one or two tokens per slot run, 32 for a few,
+// 128 for prefill.
+int token_tile(const LoraParams &p, const csgmv_batch_info &bi) {
+    const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
+    const int tps = p.num_tokens / slots;  // mean tokens per slot run
+    return tps <= 16 ? 16 : (tps <= 48 ? 32 : 128);
+}
+
+bool qkv_split_pays(const LoraParams &p, const csgmv_batch_info &bi) {
+    // the shrink-only kernel for 128-token tiles and K <= 4096, then the
+    // tcgen05 expand: measured faster than the fused kernel on prefill
+    if (token_tile(p, bi) != 128 || p.K > 4096 || p.R < 16) return false;
+    for (int j = 0; j <= p.c; ++j)
+        if (p.off[j] % 16) return false;
+    return true;
+}
+
 cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream,
                         LaunchInfo *info) {
     cudaError_t e = encoder();
@@ -438,9 +455,7 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
     const int cR = p.c * p.R;
     const int rmax = p.R <= 16 ? 16 : (p.R <= 32 ? 32 : 64);
     const int s = p.num_tokens;
-    const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
-    const int tps = s / slots;  // mean tokens per slot run
-    const int tm = tps <= 16 ? 16 : (tps <= 48 ? 32 : 128);
+    const int tm = token_tile(p, bi);
     // Prefill tiles expand on tcgen05 when every slice edge and the B rows
     // suit its operand layouts (16-column pieces, 32..128-byte swizzled rows).
     bool tc = tm == 128 && mode != kModeShrink && p.R >= 16;

@@ -67,13 +67,19 @@ def build_batch(w, chunk_override=None, graph=False, capacity=None, stream=None)
     return bi
 
 
-def run_fused(w, base=True, chunk_override=None):
-    """y = csgmv_qkv on workload w; returns (y bits, batch info)."""
+def run_fused(w, base=True, chunk_override=None, workspace=False):
+    """y = csgmv_qkv on workload w (with a workspace for h if asked);
+    returns (y bits, batch info)."""
     bi = build_batch(w, chunk_override)
     x, A, Bm = dev_bf16(w.x), dev_bf16(w.A), dev_bf16(w.B)
     y = dev_bf16(w.base) if base else torch.zeros((w.s, w.N), dtype=torch.bfloat16, device="cuda")
     widest = int(np.max(np.diff(w.offsets))) if w.c else 0
-    B.csgmv_qkv(x, A, Bm, w.offsets, w.c, widest, y, bi)
+    ws = None
+    if workspace:
+        # filled with NaN: the result must not depend on what it holds
+        ws = torch.full((B.csgmv_qkv_workspace_bytes(bi, w.c) // 4,), float("nan"), dtype=torch.float32,
+                        device="cuda")
+    B.csgmv_qkv(x, A, Bm, w.offsets, w.c, widest, y, bi, workspace=ws)
     torch.cuda.synchronize()
     return host_bits(y), bi
 

@@ -86,23 +86,23 @@ def test_host_argument_checks(lib):
     off = (ctypes.c_int32 * 4)(0, 64, 128, 192)
     P = ctypes.c_void_p(0x100000)
     # num_slices outside {1, 2, 3}
-    assert lib.csgmv_qkv(P, 64, P, P, 256, off, 4, 64, P, ctypes.byref(c), None) == INVALID
+    assert lib.csgmv_qkv(P, 64, P, P, 256, off, 4, 64, P, None, 0, ctypes.byref(c), None) == INVALID
     assert b"num_slices" in lib.csgmv_last_error()
     # offsets not multiples of 8
     bad = (ctypes.c_int32 * 2)(0, 60)
-    assert lib.csgmv_qkv(P, 64, P, P, 256, bad, 1, 64, P, ctypes.byref(c), None) == INVALID
+    assert lib.csgmv_qkv(P, 64, P, P, 256, bad, 1, 64, P, None, 0, ctypes.byref(c), None) == INVALID
     # max_slice_size below the widest slice
-    assert lib.csgmv_qkv(P, 64, P, P, 256, off, 3, 32, P, ctypes.byref(c), None) == INVALID
+    assert lib.csgmv_qkv(P, 64, P, P, 256, off, 3, 32, P, None, 0, ctypes.byref(c), None) == INVALID
     # offsets beyond N
-    assert lib.csgmv_qkv(P, 64, P, P, 128, off, 3, 64, P, ctypes.byref(c), None) == INVALID
+    assert lib.csgmv_qkv(P, 64, P, P, 128, off, 3, 64, P, None, 0, ctypes.byref(c), None) == INVALID
     # K not a multiple of 8
-    assert lib.csgmv_qkv(P, 60, P, P, 256, off, 3, 64, P, ctypes.byref(c), None) == INVALID
+    assert lib.csgmv_qkv(P, 60, P, P, 256, off, 3, 64, P, None, 0, ctypes.byref(c), None) == INVALID
     # rank above the kernels' limit
     big = _fake_bi(binding, max_rank=128)
-    assert lib.csgmv_qkv(P, 64, P, P, 256, off, 3, 64, P, ctypes.byref(big), None) == UNSUPPORTED
+    assert lib.csgmv_qkv(P, 64, P, P, 256, off, 3, 64, P, None, 0, ctypes.byref(big), None) == UNSUPPORTED
     # output overlapping the batch info
     ov = ctypes.c_void_p(0x1000)
-    assert lib.csgmv_qkv(P, 64, P, P, 256, off, 3, 64, ov, ctypes.byref(c), None) == INVALID
+    assert lib.csgmv_qkv(P, 64, P, P, 256, off, 3, 64, ov, None, 0, ctypes.byref(c), None) == INVALID
     assert b"overlaps" in lib.csgmv_last_error()
     # builder capacities
     assert lib.csgmv_build_batch_info(ctypes.byref(c), P, P, 9, 32, P, P, 4, 128, 0, 0, None) == CAPACITY

@@ -38,11 +38,14 @@ def test_lm_head_decode_full():
     assert_close(f64(y), oracle_fused(w), "lm_head decode")
 
 
-def test_prefill_gate_up_sampled():
+@pytest.mark.parametrize("workspace", [False, True], ids=["on-chip", "workspace"])
+def test_prefill_gate_up_sampled(workspace):
+    """Both csgmv_qkv paths at full size: h on chip, and the two-kernel path
+    through a workspace that the bench uses."""
     w = wl.prefill_gate_up()
     rows = sample_rows(w)
     for base in (True, False):
-        y, bi = run_fused(w, base=base)
+        y, bi = run_fused(w, base=base, workspace=workspace)
         assert bi.device_status() == 0
         assert_close(f64(y[rows]), oracle_fused(w, base=base, rows=rows), f"prefill gate_up base={base}")
 

@@ -48,6 +48,17 @@ def test_fused_matches_oracle(case):
         assert_close(f64(y), ref, f"fused base={base} {case}")
 
 
+@pytest.mark.parametrize("case", [CASES[3], CASES[4], CASES[8], CASES[9]], ids=["c1r64", "c3r64", "c2r64", "c3r32"])
+def test_fused_with_workspace_matches_oracle(case):
+    """csgmv_qkv with a workspace (two-kernel path for long slot runs) gives
+    the oracle's result, with and without base."""
+    w = make(*case)
+    for base in (True, False):
+        y, bi = run_fused(w, base=base, workspace=True)
+        assert bi.device_status() == 0
+        assert_close(f64(y), oracle_fused(w, base=base), f"fused+workspace base={base} {case}")
+
+
 def test_tiny_single_slice_workload():
     w = wl.tiny_single_slice()
     for base in (True, False):
