@@ -205,6 +205,31 @@ CSGMV_API int csgmv_qkv(const void *x, int64_t K, const void *A, const void *B, 
 CSGMV_API size_t csgmv_qkv_workspace_bytes(const csgmv_batch_info *bi, int num_slices);
 
 /*
+ * csgmv_qkv for callers that cannot allocate device memory when they call it
+ * (no counterpart on the pages: an addition of this library).  Some callers
+ * cannot call cudaMalloc or a caching allocator at that point (for instance
+ * code whose device memory is planned up front by an engine that owns every
+ * buffer), so they cannot provide csgmv_qkv's workspace.  This entry point
+ * takes the same arguments without one and uses a fixed 32 MiB array in the
+ * library's own device memory as the h workspace; the library allocates
+ * nothing and frees nothing here either.
+ *   - Limit: the batch's h, num_tokens * num_slices * max_rank * 4 bytes,
+ *     must fit in 32 MiB, else CSGMV_ERR_CAPACITY (nothing is launched).
+ *   - Every GPU that loads the library holds the 32 MiB until the process
+ *     exits.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before capturing the stream.
+ *   - All calls share the one array: two calls that may run at the same time
+ *     on the GPU (different streams, or unordered graph branches) race on it.
+ *     Nothing in it has to start at zero; the shrink writes every h row the
+ *     expand reads.
+ */
+CSGMV_API int csgmv_qkv_static_scratch(const void *x, int64_t K, const void *A, const void *B, int64_t N,
+                             const int32_t *slice_offsets, int num_slices, int max_slice_size,
+                             void *base_output, const csgmv_batch_info *bi, csgmv_stream_t stream);
+
+/*
  * Embedding LoRA-A gather (base_backend.py run_lora_a_embedding;
  * chunked_backend.py run_lora_a_embedding, which takes no extra-token
  * embeddings): for token t on slot w with rank r,

@@ -23,7 +23,7 @@ STATUS_BITS = {
 
 EXPORTED = ["csgmv_last_error", "csgmv_version", "csgmv_chunk_size", "csgmv_batch_info_capacity",
             "csgmv_build_batch_info", "csgmv_shrink", "csgmv_expand", "csgmv_qkv", "csgmv_qkv_workspace_bytes",
-            "embedding_lora_a"]
+            "csgmv_qkv_static_scratch", "embedding_lora_a"]
 
 
 class CsgmvError(RuntimeError):
@@ -66,6 +66,7 @@ def lib():
         "csgmv_expand": (i32, [vp, i32, i64, vp, i64, i32p, i32, i32, vp, i32, bip, vp]),
         "csgmv_qkv": (i32, [vp, i64, vp, vp, i64, i32p, i32, i32, vp, vp, ctypes.c_size_t, bip, vp]),
         "csgmv_qkv_workspace_bytes": (ctypes.c_size_t, [bip, i32]),
+        "csgmv_qkv_static_scratch": (i32, [vp, i64, vp, vp, i64, i32p, i32, i32, vp, bip, vp]),
         "embedding_lora_a": (i32, [vp, vp, i64, i32, vp, bip, vp]),
     }
     for name, (res, args) in sig.items():
@@ -209,6 +210,19 @@ def csgmv_qkv(x: torch.Tensor, A: torch.Tensor, B: torch.Tensor, slice_offsets, 
 
 def csgmv_qkv_workspace_bytes(bi: BatchInfo, num_slices: int) -> int:
     return int(lib().csgmv_qkv_workspace_bytes(ctypes.byref(bi.c), int(num_slices)))
+
+
+def csgmv_qkv_static_scratch(x: torch.Tensor, A: torch.Tensor, B: torch.Tensor, slice_offsets, num_slices: int,
+                             max_slice_size: int, base_output: torch.Tensor, bi: BatchInfo,
+                             stream=None) -> torch.Tensor:
+    """csgmv_qkv with the library's own fixed device scratch for h, for
+    callers that cannot allocate a workspace (see csgmv.h)."""
+    K = int(x.shape[1])
+    N = int(base_output.shape[1])
+    _check(lib().csgmv_qkv_static_scratch(_ptr(x), K, _ptr(A), _ptr(B), N, _offsets(slice_offsets),
+                                          int(num_slices), int(max_slice_size), _ptr(base_output),
+                                          ctypes.byref(bi.c), _stream(stream)))
+    return base_output
 
 
 def embedding_lora_a(input_ids: torch.Tensor, A_emb: torch.Tensor, vocab_size: int, out: torch.Tensor,

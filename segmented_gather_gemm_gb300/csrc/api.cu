@@ -28,6 +28,17 @@ int cuda_fail(cudaError_t e, const char *what) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+namespace csgmv {
+int set_error(int code, const char *msg) {
+    g_last_error = msg;
+    return code;
+}
+}  // namespace csgmv
+
+namespace {
+
 bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes) {
     if (!a || !b || abytes == 0 || bbytes == 0) return false;
     uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);

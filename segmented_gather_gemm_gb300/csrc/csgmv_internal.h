@@ -53,6 +53,9 @@ struct LaunchInfo {
 // lora.cu
 cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream,
                         LaunchInfo *info);
+// Record `msg` as this thread's csgmv_last_error() and return `code`.
+int set_error(int code, const char *msg);
+
 // Whether csgmv_qkv should run as shrink + expand through a workspace.
 bool qkv_split_pays(const LoraParams &p, const csgmv_batch_info &bi);
 

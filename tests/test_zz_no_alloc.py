@@ -1,0 +1,63 @@
+"""csgmv_qkv_static_scratch: csgmv_qkv for callers that cannot allocate a
+workspace when they call it.
+
+Such callers (an engine that plans all device memory up front and hands the
+kernel only its own tensors, or code that must not call cudaMalloc or a
+caching allocator at that point) still get the two-kernel prefill path: the
+library keeps a fixed 32 MiB device array for h.  These tests run it through
+the C ABI on two different batches in a row, so that anything a call left in
+the shared array would show up in the next one, and compare each result with
+csgmv_qkv given an ordinary workspace.  This file sorts last so that a run
+that stops at its first failure has already run every other test.
+"""
+import numpy as np
+import pytest
+import torch
+
+from segmented_gather_gemm_gb300 import binding as B
+from segmented_gather_gemm_gb300 import workloads as wl
+from tests.gpu_helpers import assert_close, build_batch, dev_bf16, host_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _prefill_case(seed):
+    # long runs per slot (128-token tiles), K <= 4096, R >= 16 and slice edges
+    # on 16-column boundaries: csgmv_qkv runs shrink + expand through h
+    return wl.random_lora(seed, bs=3, max_len=700, K=256, N_slices=[128, 64, 64], R=32, L=3,
+                          rank_choices=list(range(1, 33)), zero_rank_prob=0.2, std=0.5, min_len=200)
+
+
+def _run(w, static):
+    bi = build_batch(w)
+    x, A, Bm, y = dev_bf16(w.x), dev_bf16(w.A), dev_bf16(w.B), dev_bf16(w.base)
+    widest = int(np.max(np.diff(w.offsets)))
+    if static:
+        B.csgmv_qkv_static_scratch(x, A, Bm, w.offsets, w.c, widest, y, bi)
+    else:
+        ws = torch.full((B.csgmv_qkv_workspace_bytes(bi, w.c) // 4,), float("nan"), dtype=torch.float32,
+                        device="cuda")
+        B.csgmv_qkv(x, A, Bm, w.offsets, w.c, widest, y, bi, workspace=ws)
+    torch.cuda.synchronize()
+    assert bi.device_status() == 0
+    return host_f64(y)
+
+
+def test_static_scratch_matches_csgmv_qkv_on_two_calls_in_a_row():
+    for seed in (11, 12):  # the second call finds the first call's h in the array
+        w = _prefill_case(seed)
+        got = _run(w, static=True)
+        ref = _run(w, static=False)
+        assert_close(got, ref, f"static scratch vs csgmv_qkv, seed {seed}")
+
+
+def test_static_scratch_rejects_a_batch_too_large_for_it():
+    # 50000 tokens x 3 slices x rank 64 x 4 bytes of h exceed the 32 MiB array;
+    # the call is refused before anything is launched
+    bi = B.BatchInfo.for_batch(1, 50000, 1, 64)
+    bi.c.num_tokens = 50000
+    t = torch.zeros((8, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(B.CsgmvError) as err:
+        B.csgmv_qkv_static_scratch(t, t, t, [0, 64, 128, 192], 3, 64, t, bi)
+    assert err.value.code == -2
+    assert "static scratch" in str(err.value)
