@@ -69,9 +69,22 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
     int *flags = warp_sums + kWarps;    // [0] error bits, [1] nseg
 
     const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
     const int chunk = p.chunk;
+    int *wsum = flags + 2;  // [kWarps][L] per-warp token totals of each slot
+    // Up to 1024 requests (one per thread) take one pass: each thread loads its
+    // request once and keeps it in registers for the counts, the offsets and
+    // its destination.
+    const bool one_tile = p.bs <= kBuildThreads;
+    int my_a = -1, my_l = 0;
+    if (one_tile && tid < p.bs) {
+        my_a = p.req_adapter[tid];
+        my_l = p.req_lens[tid];
+    }
     if (tid == 0) { flags[0] = 0; flags[1] = 0; }
     for (int a = tid; a < L; a += kBuildThreads) cnt[a] = 0;
+    if (one_tile)
+        for (int x = tid; x < kWarps * L; x += kBuildThreads) wsum[x] = 0;
     __syncthreads();
 
     // Slot table (lora_manager.py prepare_lora_batch: lora_ranks / scalings per slot).
@@ -88,22 +101,48 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
     }
 
     // Per-slot token counts and validation.
-    for (int i = tid; i < p.bs; i += kBuildThreads) {
-        int a = p.req_adapter[i], l = p.req_lens[i];
-        if (a < 0 || a >= p.num_loras) atomicOr(&flags[0], CSGMV_STATUS_BAD_ADAPTER);
-        else if (l < 0) atomicOr(&flags[0], CSGMV_STATUS_BAD_LENS);
-        else atomicAdd(&cnt[a], l);
+    int my_pre = 0;  // one pass: tokens of earlier requests of this warp on the same slot
+    if (one_tile) {
+        const bool valid = tid < p.bs;
+        if (valid) {
+            if (my_a < 0 || my_a >= p.num_loras) atomicOr(&flags[0], CSGMV_STATUS_BAD_ADAPTER);
+            else if (my_l < 0) atomicOr(&flags[0], CSGMV_STATUS_BAD_LENS);
+            else atomicAdd(&cnt[my_a], my_l);
+        }
+        bool last = true;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const int ak = __shfl_sync(0xffffffffu, my_a, k);
+            const int lk = __shfl_sync(0xffffffffu, my_l, k);
+            if (ak == my_a && k < lane) my_pre += lk;
+            if (ak == my_a && k > lane) last = false;
+        }
+        if (valid && last && my_a >= 0 && my_a < L) wsum[warp * L + my_a] = my_pre + my_l;
+    } else {
+        for (int i = tid; i < p.bs; i += kBuildThreads) {
+            int a = p.req_adapter[i], l = p.req_lens[i];
+            if (a < 0 || a >= p.num_loras) atomicOr(&flags[0], CSGMV_STATUS_BAD_ADAPTER);
+            else if (l < 0) atomicOr(&flags[0], CSGMV_STATUS_BAD_LENS);
+            else atomicAdd(&cnt[a], l);
+        }
     }
 
     // req_start = [0, cumsum(lens)] (chunked_backend.py _build_req_seg_indptr).
     int carry = 0;
-    for (int i0 = 0; i0 < p.bs; i0 += kBuildThreads) {
-        int i = i0 + tid;
-        int l = (i < p.bs) ? max(p.req_lens[i], 0) : 0;
+    if (one_tile) {
         int tot;
-        int pre = block_exclusive_scan(l, warp_sums, &tot);
-        if (i < p.bs) req_start[i] = carry + pre;
-        carry += tot;
+        const int pre = block_exclusive_scan(tid < p.bs ? max(my_l, 0) : 0, warp_sums, &tot);
+        if (tid < p.bs) req_start[tid] = pre;
+        carry = tot;
+    } else {
+        for (int i0 = 0; i0 < p.bs; i0 += kBuildThreads) {
+            int i = i0 + tid;
+            int l = (i < p.bs) ? max(p.req_lens[i], 0) : 0;
+            int tot;
+            int pre = block_exclusive_scan(l, warp_sums, &tot);
+            if (i < p.bs) req_start[i] = carry + pre;
+            carry += tot;
+        }
     }
     if (tid == 0) {
         req_start[p.bs] = carry;
@@ -150,41 +189,53 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
     // Destination of every request: stable within a slot, so earlier requests
     // on the same slot come first.  Per 1024-request tile: lanes of a warp
     // with the same slot add up their predecessors' lengths, the last such
-    // lane posts the warp's total for the slot, and one thread per slot turns
-    // the warp totals into running offsets (three barriers per tile).
-    const int lane = tid & 31, warp = tid >> 5;
-    int *wsum = flags + 2;  // [kWarps][L]
-    for (int i0 = 0; i0 < p.bs; i0 += kBuildThreads) {
-        int i = i0 + tid;
-        bool valid = i < p.bs;
-        int a = valid ? p.req_adapter[i] : -1;
-        int l = valid ? p.req_lens[i] : 0;
-        int pre = 0;
-        bool last = true;
+    // lane posts the warp's total for the slot, and one warp per slot scans
+    // the warp totals into running offsets.
+    auto slot_scan = [&]() {
+        for (int b = warp; b < L; b += kWarps) {  // one warp per slot: scan over the 32 warps
+            const int v = wsum[lane * L + b];
+            int inc = v;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            int ak = __shfl_sync(0xffffffffu, a, k);
-            int lk = __shfl_sync(0xffffffffu, l, k);
-            if (ak == a && k < lane) pre += lk;
-            if (ak == a && k > lane) last = false;
-        }
-        for (int x = tid; x < kWarps * L; x += kBuildThreads) wsum[x] = 0;
-        __syncthreads();
-        if (valid && last) wsum[warp * L + a] = pre + l;
-        __syncthreads();
-        for (int b = tid; b < L; b += kBuildThreads) {
-            int running = run[b];
-            for (int w = 0; w < kWarps; ++w) {
-                const int v = wsum[w * L + b];
-                wsum[w * L + b] = running;
-                running += v;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += n;
             }
-            run[b] = running;
+            const int base = run[b];
+            wsum[lane * L + b] = base + inc - v;
+            __syncwarp();
+            if (lane == 31) run[b] = base + inc;
         }
+    };
+    if (one_tile) {
+        slot_scan();  // the warp totals were posted in the counting pass
         __syncthreads();
-        if (valid) req_dest[i] = wsum[warp * L + a] + pre;
-        __syncthreads();  // wsum is reused by the next tile
+        if (tid < p.bs) req_dest[tid] = wsum[warp * L + my_a] + my_pre;
+    } else {
+        for (int i0 = 0; i0 < p.bs; i0 += kBuildThreads) {
+            int i = i0 + tid;
+            bool valid = i < p.bs;
+            int a = valid ? p.req_adapter[i] : -1;
+            int l = valid ? p.req_lens[i] : 0;
+            int pre = 0;
+            bool last = true;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                int ak = __shfl_sync(0xffffffffu, a, k);
+                int lk = __shfl_sync(0xffffffffu, l, k);
+                if (ak == a && k < lane) pre += lk;
+                if (ak == a && k > lane) last = false;
+            }
+            for (int x = tid; x < kWarps * L; x += kBuildThreads) wsum[x] = 0;
+            __syncthreads();
+            if (valid && last) wsum[warp * L + a] = pre + l;
+            __syncthreads();
+            slot_scan();
+            __syncthreads();
+            if (valid) req_dest[i] = wsum[warp * L + a] + pre;
+            __syncthreads();  // wsum is reused by the next tile
+        }
     }
+    __syncthreads();
 
     // Segments (chunked_backend.py _get_segments_info): slot runs in ascending
     // slot order, each cut into ceil(n / chunk) pieces of chunk tokens, the
