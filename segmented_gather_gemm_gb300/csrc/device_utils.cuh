@@ -145,6 +145,12 @@ __device__ __forceinline__ void tma_scatter4(const void *tmap, int x, int y0, in
         "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(src))
         : "memory");
 }
+// 2D tiled store of a shared-memory box (bulk async-group completion).
+__device__ __forceinline__ void tma_store_2d(const void *tmap, int x, int y, const void *src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(tmap),
+                 "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {

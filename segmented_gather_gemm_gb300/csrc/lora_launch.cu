@@ -129,7 +129,7 @@ size_t carve(TmaKernelParams &k, int mode, int tm, int cs, int S1, int S2, bool 
     k.a_rows = (int)align_up((size_t)cR, 16);
     k.o_bar = take((size_t)(2 * k.S1 + 2 * k.S2) * 8, 8);
     k.o_tc = tc ? take(64, 16) : 0;
-    const size_t ah_bytes = tc ? (size_t)k.p.c * 2 * kTcAhBytes : 0;
+    const size_t ah_bytes = tc ? (size_t)k.ah_slices * 2 * kTcAhBytes : 0;
     k.o_run = take((size_t)(5 * k.runcap + 1 + 32) * 4, 16);
     k.o_tok = take((size_t)tm * 4, 16);
     if (mode != kModeExpand) {
@@ -198,6 +198,25 @@ size_t carve_ws(TmaKernelParams &k, int mode, int S1, int S2) {
     }
     // at least 116 KB, so that one CTA holds an SM (and its 512 TMEM columns)
     return std::max(off, (size_t)116 * 1024);
+}
+
+// Most slices that one CTA's column range spans, for nsplit * cs column
+// parts (the device split in column_range()).
+int max_slice_span(const LoraParams &p, int parts) {
+    const int ntot = p.off[p.c] - p.off[0];
+    const int nblk = (ntot + 63) / 64;
+    auto slice_of = [&](int col) {
+        int j = 0;
+        while (j + 1 < p.c && col >= p.off[j + 1]) ++j;
+        return j;
+    };
+    int span = 1;
+    for (int part = 0; part < parts; ++part) {
+        const int b0 = (int)((int64_t)part * nblk / parts), b1 = (int)((int64_t)(part + 1) * nblk / parts);
+        const int n0 = p.off[0] + 64 * b0, n1 = std::min(p.off[p.c], p.off[0] + 64 * b1);
+        if (n1 > n0) span = std::max(span, slice_of(n1 - 1) - slice_of(n0) + 1);
+    }
+    return span;
 }
 
 // Shared-memory carve-up of the small-tile kernel.
@@ -482,6 +501,7 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
     k.p = p;
     k.max_segments = bi.max_segments;
     k.runcap = std::max(1, std::min(bi.max_segments, bi.max_loras + std::max(bi.max_bs, 1)));
+    k.ah_slices = p.c;  // until the column split is known
     const size_t budget = 227 * 1024;
     const int nkc = (int)((p.K + 63) / 64);
     const int nb64 = tc ? kTcCols / 64 : (tm >= 128 ? 1 : (tm >= 64 ? 2 : 4));
@@ -537,6 +557,21 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
         const int max_split = std::max(1, nblk / (cs * nb64));
         k.p.nsplit = std::max(1, std::min(best_res / std::max(tiles_ub, 1), max_split));
     }
+    if (tc && mode == kModeExpand && p.c > 1) {
+        // At least one column block per slice, so that a CTA's columns mostly
+        // stay within one slice: then the h operand tiles of fewer slices are
+        // needed, and the room goes to more expand stages in flight.
+        const int nblk = (p.off[p.c] - p.off[0] + 63) / 64;
+        k.p.nsplit = std::max(k.p.nsplit, std::min(p.c, std::max(1, nblk / nb64)));
+        k.ah_slices = max_slice_span(k.p, k.p.nsplit * cs);
+        int S2 = 8;
+        smem = carve(k, mode, tm, cs, 1, S2, tc);
+        while (smem > budget && S2 > 2) smem = carve(k, mode, tm, cs, 1, --S2, tc);
+        if (smem > budget) return cudaErrorInvalidConfiguration;
+    } else if (tc) {
+        k.ah_slices = max_slice_span(k.p, k.p.nsplit * cs);
+        if (k.ah_slices < p.c) smem = carve(k, mode, tm, cs, k.S1, k.S2, tc);
+    }
     const int64_t units_ub = (int64_t)tiles_ub * k.p.nsplit;
     const int nclusters = (int)std::max<int64_t>(1, std::min<int64_t>(best_res, units_ub));
 
@@ -561,7 +596,7 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
                              CU_TENSOR_MAP_SWIZZLE_128B);
     else
         k.tmX = k.tmA;
-    if (k.row_tma && mode != kModeShrink && p.accumulate)
+    if (k.row_tma && mode != kModeShrink)  // base loads (accumulating) and whole-tile stores
         ok = ok && encode_2d(&k.tmY, p.y, (uint64_t)p.N, (uint64_t)s, (uint64_t)p.N * 2, 64, tm,
                              CU_TENSOR_MAP_SWIZZLE_128B);
     else

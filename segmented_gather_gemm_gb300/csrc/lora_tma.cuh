@@ -65,6 +65,7 @@ struct TmaKernelParams {
     int hp;            // floats per hpart / hred row
     int o_tc;          // tensor-core expand: acc_full[2], acc_empty[2], TMEM base address
     int o_ah;          // tensor-core expand: h of every slice as bf16 hi / lo operand tiles
+    int ah_slices;     // tensor-core expand: slices one CTA's column range can span (operand tile pairs)
     int o_bring;       // warp-specialized kernel: B tiles of the expand stages (consecutive slots)
     int xpitch, ypitch;  // small-tile kernel: bytes per staged x row / base row
     int kc_per;          // small-tile kernel: 64-wide K chunks staged per CTA
@@ -290,12 +291,20 @@ __device__ void expand_tc(const TmaKernelParams &k, unsigned char *smem, const U
     const float *hred = reinterpret_cast<const float *>(smem + k.o_hred);
     const int hp = k.hp;
 
-    // h of every slice: operand tile 2j (hi) and 2j+1 (lo), row m = token m of
-    // the tile, columns [0, RK) of which [r, RK) are zero.
+    // h of every slice this CTA's columns touch (slices jfirst..): operand tile
+    // 2(j - jfirst) (hi) and 2(j - jfirst) + 1 (lo), row m = token m of the
+    // tile, columns [0, RK) of which [r, RK) are zero.
+    const int jfirst = slice_at(p, n0);
+    const int nsl = slice_at(p, n1 - 1) - jfirst + 1;
+    if (nsl > k.ah_slices) {  // the launcher sized the tiles for fewer slices: refuse the unit
+        if (tid == 0) atomicOr(p.status, kStatusTimeout);
+        return;
+    }
     const int cpr = RK / 8;
     const int per_slice = TM * cpr;
-    for (int idx = tid; idx < p.c * per_slice; idx += kConsumerThreads) {
-        const int j = idx / per_slice, rem = idx % per_slice;
+    for (int idx = tid; idx < nsl * per_slice; idx += kConsumerThreads) {
+        const int jo = idx / per_slice, rem = idx % per_slice;
+        const int j = jfirst + jo;
         const int m = rem / cpr, ch = rem % cpr;
         float v[8];
 #pragma unroll
@@ -322,8 +331,8 @@ __device__ void expand_tc(const TmaKernelParams &k, unsigned char *smem, const U
         split_pair(v[4], v[5], hi.z, lo.z);
         split_pair(v[6], v[7], hi.w, lo.w);
         const int off = m * 128 + ((ch ^ (m & 7)) << 4);
-        *reinterpret_cast<uint4 *>(ah + (2 * j) * kTcAhBytes + off) = hi;
-        *reinterpret_cast<uint4 *>(ah + (2 * j + 1) * kTcAhBytes + off) = lo;
+        *reinterpret_cast<uint4 *>(ah + (2 * jo) * kTcAhBytes + off) = hi;
+        *reinterpret_cast<uint4 *>(ah + (2 * jo + 1) * kTcAhBytes + off) = lo;
     }
     fence_proxy_async_smem();  // the operand tiles are read by the tensor core
     __syncthreads();
@@ -363,7 +372,8 @@ __device__ void expand_tc(const TmaKernelParams &k, unsigned char *smem, const U
                 const int c1 = j + 1 < p.c ? min(ncols, p.off[j + 1] - x0) : ncols;
                 const uint32_t idesc = idesc_bf16_f32(128, c1 - c0);
                 const uint32_t d = tmem + (uint32_t)(a * kTcCols + c0);
-                const uint32_t ahi = smem_u32(ah + (2 * j) * kTcAhBytes), alo = smem_u32(ah + (2 * j + 1) * kTcAhBytes);
+                const int jo = j - jfirst;
+                const uint32_t ahi = smem_u32(ah + (2 * jo) * kTcAhBytes), alo = smem_u32(ah + (2 * jo + 1) * kTcAhBytes);
                 for (int ks = 0; ks < ksteps; ++ks) {
                     const uint64_t bd = smem_desc_kmajor(bsa + (uint32_t)(c0 * Rb + ks * 32), Rb);
                     tc_mma_bf16(d, smem_desc_kmajor(ahi + ks * 32, 128), bd, idesc, ks > 0);

@@ -79,11 +79,6 @@ __device__ __forceinline__ WsBars ws_bars(const TmaKernelParams &k, unsigned cha
     return w;
 }
 
-__device__ __forceinline__ void tma_store_2d(const void *tmap, int x, int y, const void *src) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(tmap),
-                 "r"(x), "r"(y), "r"(smem_u32(src))
-                 : "memory");
-}
 
 // The same unit walk on every role: unit, rank, column range and stage count;
 // false when the unit has no work for the tensor-core roles.
