@@ -78,6 +78,9 @@ def _bind(lib):
                                             ctypes.c_int, _i32p, _i32p, _i32p, _i32p, _i32p,
                                             _i32p, _i32p]
     lib.oracle_shrink.restype = ctypes.c_int
+    lib.oracle_build_lm_head_batch_info.argtypes = [_i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int, _i32p, _i32p, _i32p, _i32p]
+    lib.oracle_build_lm_head_batch_info.restype = ctypes.c_int
     lib.oracle_shrink.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int64, _u16p, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_int, _i32p, _i32p, _f64p]
     lib.oracle_expand.restype = ctypes.c_int
@@ -132,6 +135,33 @@ def token_adapter(req_lens, req_adapter) -> np.ndarray:
     out = np.zeros(max(int(lens.sum()), 1), np.int32)
     n = _load().oracle_token_adapter(_p(lens, _i32p), _p(ad, _i32p), len(lens), _p(out, _i32p))
     return out[:n]
+
+
+def build_lm_head_batch_info(pruned_lens, req_adapter, chunk: int, use_cuda_graph: bool = False,
+                             max_segments: int | None = None) -> dict:
+    """Pruned lm_head batch info (identity permutation), as numpy int32 arrays."""
+    lens = _c(pruned_lens, np.int32)
+    ad = _c(req_adapter, np.int32)
+    bs = len(lens)
+    s = int(lens.sum())
+    if max_segments is None:
+        max_segments = max(s, 1)
+    perm = np.zeros(max(s, 1), np.int32)
+    wi = np.full(max(max_segments, 1), -7, np.int32)
+    indptr = np.full(max_segments + 1, -7, np.int32)
+    nseg = ctypes.c_int32(0)
+    rc = _load().oracle_build_lm_head_batch_info(
+        _p(lens, _i32p), _p(ad, _i32p), bs, int(chunk), int(bool(use_cuda_graph)), int(max_segments),
+        _p(perm, _i32p), _p(wi, _i32p), _p(indptr, _i32p), ctypes.byref(nseg))
+    n = int(nseg.value)
+    out = dict(rc=int(rc), num_segments=n, permutation=perm[:s].copy(), chunk=int(chunk), num_tokens=s)
+    if use_cuda_graph:
+        out["weight_indices"] = wi[:max_segments].copy()
+        out["seg_indptr"] = indptr.copy()
+    else:
+        out["weight_indices"] = wi[:n].copy()
+        out["seg_indptr"] = indptr[:n + 1].copy()
+    return out
 
 
 def build_batch_info(req_lens, req_adapter, chunk: int, use_cuda_graph: bool = False,

@@ -202,6 +202,64 @@ int oracle_build_batch_info(const int32_t *req_lens, const int32_t *req_adapter,
 }
 
 /* ------------------------------------------------------------------------- *
+ * Pruned lm_head batch info.  [CB] _prepare_lm_head_batch_info and
+ * _build_lm_head_batch_info: only pruned_lens[i] tokens of request i reach
+ * lm_head, kept in their original order (identity permutation);
+ * merge_and_chunk_segments(weight_indices, pruned_lens, chunk_size) gives the
+ * segments.  Its body is not on the pages; read from its call sites:
+ *   1. walk the requests in order, skipping those without pruned tokens, and
+ *      merge each request into the previous run when both use the same slot;
+ *   2. cut every run into pieces of chunk tokens, the last one shorter.
+ * Returns 0, or -1 when the segments exceed max_segments (then 0 segments).
+ * ------------------------------------------------------------------------- */
+int oracle_build_lm_head_batch_info(const int32_t *pruned_lens, const int32_t *req_adapter, int bs, int chunk,
+                                    int use_cuda_graph, int max_segments, int32_t *permutation,
+                                    int32_t *weight_indices, int32_t *seg_indptr, int32_t *num_segments)
+{
+    /* step 1: runs of consecutive non-empty requests on one slot */
+    int32_t *run_slot = (int32_t *)malloc(sizeof(int32_t) * (size_t)(bs > 0 ? bs : 1));
+    int32_t *run_len = (int32_t *)malloc(sizeof(int32_t) * (size_t)(bs > 0 ? bs : 1));
+    int nruns = 0, s = 0;
+    for (int i = 0; i < bs; ++i) {
+        if (pruned_lens[i] == 0) continue;
+        if (nruns > 0 && run_slot[nruns - 1] == req_adapter[i]) {
+            run_len[nruns - 1] += pruned_lens[i];
+        } else {
+            run_slot[nruns] = req_adapter[i];
+            run_len[nruns] = pruned_lens[i];
+            ++nruns;
+        }
+        s += pruned_lens[i];
+    }
+    /* step 2: chunks of every run */
+    int nseg = 0, rc = 0, cum = 0;
+    seg_indptr[0] = 0;
+    for (int k = 0; k < nruns && !rc; ++k) {
+        int left = run_len[k];
+        while (left > 0) {
+            int len = left < chunk ? left : chunk;
+            if (nseg >= max_segments) { rc = -1; break; }
+            weight_indices[nseg] = run_slot[k];
+            cum += len;
+            seg_indptr[nseg + 1] = cum;
+            ++nseg;
+            left -= len;
+        }
+    }
+    for (int t = 0; t < s; ++t) permutation[t] = t;
+    *num_segments = rc ? 0 : nseg;
+    if (!rc && use_cuda_graph) {
+        for (int k = nseg; k < max_segments; ++k) {  /* padding: zero-length segments at the end */
+            weight_indices[k] = 0;
+            seg_indptr[k + 1] = cum;
+        }
+    }
+    free(run_slot);
+    free(run_len);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------- *
  * Shrink.  [BB] run_lora_a_sgemm: x (s, K), A (L, c*R, K) -> h (s, c*R), and
  * [CB] run_lora_a_sgemm / run_qkv_lora / run_gate_up_lora (num_slices = c).
  * For token t with slot w and rank r:

@@ -30,6 +30,11 @@ MUTATIONS = [
     ("graph_padding_value", "seg_indptr[k + 1] = s;", "seg_indptr[k + 1] = 0;", ["tiny"]),
     ("embedding_ignores_rank", "for (int k = 0; k < r && k < R; ++k)", "for (int k = 0; k < R; ++k)",
      ["embedding"]),
+    ("lm_head_empty_request_breaks_run", "if (pruned_lens[i] == 0) continue;",
+     "if (pruned_lens[i] == 0) { run_slot[nruns] = -1; run_len[nruns] = 0; ++nruns; continue; }",
+     ["lm_head"]),
+    ("lm_head_no_merge", "if (nruns > 0 && run_slot[nruns - 1] == req_adapter[i]) {",
+     "if (nruns < 0) {", ["lm_head"]),
     ("expand_uses_max_rank", "for (int k = 0; k < r; ++k)\n                    acc += ht",
      "for (int k = 0; k < R; ++k)\n                    acc += ht", ["fused_dense", "padding"]),
 ]
@@ -44,6 +49,7 @@ PINS = {
     "embedding": pins.test_embedding_is_column_indexing,
     "rank0": pins.test_rank_zero_and_no_adapter_leave_base_exact,
     "padding": pins.test_padding_is_never_read,
+    "lm_head": pins.test_lm_head_batch_info_hand_derived,
 }
 
 

@@ -145,6 +145,48 @@ def test_builder_invariants(seed):
         assert got == counts[a]
 
 
+def test_lm_head_batch_info_hand_derived():
+    g = golden("lm_head_batch_info.json")
+    bi = oracle.build_lm_head_batch_info(g["pruned_lens"], g["req_adapter"], chunk=g["chunk_size"])
+    assert bi["rc"] == 0
+    assert bi["permutation"].tolist() == g["permutation"]
+    assert bi["weight_indices"].tolist() == g["weight_indices"]
+    assert bi["seg_indptr"].tolist() == g["seg_indptr"]
+    gb = oracle.build_lm_head_batch_info(g["pruned_lens"], g["req_adapter"], chunk=g["chunk_size"],
+                                         use_cuda_graph=True, max_segments=g["graph_max_segments"])
+    assert gb["weight_indices"].tolist() == g["graph_weight_indices"]
+    assert gb["seg_indptr"].tolist() == g["graph_seg_indptr"]
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_lm_head_batch_info_invariants(seed):
+    """Segments of a pruned lm_head batch, checked token by token: they tile
+    [0, s) in order, each holds tokens of one slot only and at most `chunk` of
+    them, and a segment ends early only where the slot changes (maximal runs,
+    empty requests ignored)."""
+    rng = np.random.default_rng(3000 + seed)
+    bs = int(rng.integers(1, 80))
+    L = int(rng.integers(1, 6))
+    lens = rng.integers(0, 6, size=bs) * (rng.random(bs) < 0.7)
+    adapter = rng.integers(0, L, size=bs)
+    s = int(lens.sum())
+    chunk = int(rng.choice([1, 2, 3, 4, 16]))
+    bi = oracle.build_lm_head_batch_info(lens, adapter, chunk=chunk)
+    assert bi["rc"] == 0
+    assert bi["permutation"].tolist() == list(range(s))
+    key = np.repeat(adapter, lens)  # slot of every pruned token, in order
+    n, indptr, wi = bi["num_segments"], bi["seg_indptr"], bi["weight_indices"]
+    assert indptr[0] == 0 and indptr[n] == s
+    for k in range(n):
+        a, b = indptr[k], indptr[k + 1]
+        assert 1 <= b - a <= chunk
+        assert np.all(key[a:b] == wi[k])
+        if k + 1 < n and wi[k + 1] == wi[k]:
+            assert b - a == chunk  # same slot continues: this piece is full
+        if k + 1 < n and wi[k + 1] != wi[k]:
+            assert key[b] != key[b - 1]
+
+
 def test_builder_capacity_overflow_reports():
     bi = oracle.build_batch_info([40, 40], [0, 1], chunk=16, use_cuda_graph=True, max_segments=3)
     assert bi["rc"] == -1 and bi["num_segments"] == 0
