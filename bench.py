@@ -47,6 +47,8 @@ def make_workload(name: str, seed: int, chunk: int, scale: float = 1.0, bs: int 
         return wl.skewed_down_proj(seed=seed, chunk=chunk, scale_tokens=scale)
     if name == "lm_head_decode":
         return wl.lm_head_decode(seed=seed, bs=bs or 512)
+    if name == "lm_head_pruned":
+        return wl.lm_head_pruned(seed=seed, bs=bs or 64)
     if name == "tiny":
         return wl.tiny_single_slice(seed=seed)
     if name == "embedding":
@@ -218,7 +220,10 @@ class DeviceSet:
         else:
             self.scal = torch.from_numpy(w.scalings).cuda()
             self.x, self.A, self.B, self.y = bf(w.x), bf(w.A), bf(w.B), bf(w.base)
-            self.bi = B.BatchInfo.for_batch(w.bs, w.s, w.L, w.R, min_chunk=min(16, chunk_override or 16))
+            if w.meta.get("builder") == "lm_head":  # runs in request order: room for one segment per token
+                self.bi = B.BatchInfo(w.bs, w.s, w.s + 1, max_loras=w.L, max_rank=w.R)
+            else:
+                self.bi = B.BatchInfo.for_batch(w.bs, w.s, w.L, w.R, min_chunk=min(16, chunk_override or 16))
             self.widest = int(np.max(np.diff(w.offsets)))
             # h workspace: csgmv_qkv takes its two-kernel path where that is faster
             self.ws = torch.empty(B.csgmv_qkv_workspace_bytes(self.bi, w.c) // 4, dtype=torch.float32,
@@ -228,6 +233,10 @@ class DeviceSet:
     def build(self):
         from segmented_gather_gemm_gb300 import binding as B
         w = self.w
+        if getattr(w, "meta", {}).get("builder") == "lm_head":
+            B.csgmv_build_lm_head_batch_info(self.bi, self.lens, self.ad, w.s, self.ranks, self.scal,
+                                             max_chunk_size=w.max_chunk_size, use_cuda_graph=True)
+            return
         B.csgmv_build_batch_info(self.bi, self.lens, self.ad, w.s, self.ranks, self.scal,
                                  max_chunk_size=w.max_chunk_size, chunk_size_override=self.chunk_override,
                                  use_cuda_graph=True)
@@ -443,7 +452,9 @@ def run_e2e(torch, w, chunk_override, steps, world):
     da = torch.empty_like(had, device="cuda")
     dr = torch.empty_like(hranks, device="cuda")
     ds = torch.empty_like(hscal, device="cuda")
-    bi = B.BatchInfo.for_batch(w.bs, w.s, w.L, w.R)
+    lm_head = w.meta.get("builder") == "lm_head"
+    bi = B.BatchInfo(w.bs, w.s, w.s + 1, max_loras=w.L, max_rank=w.R) if lm_head \
+        else B.BatchInfo.for_batch(w.bs, w.s, w.L, w.R)
     widest = int(np.max(np.diff(w.offsets)))
     ws = torch.empty(B.csgmv_qkv_workspace_bytes(bi, w.c) // 4, dtype=torch.float32, device="cuda")
 
@@ -454,8 +465,11 @@ def run_e2e(torch, w, chunk_override, steps, world):
         da.copy_(had, non_blocking=True)
         dr.copy_(hranks, non_blocking=True)
         ds.copy_(hscal, non_blocking=True)
-        B.csgmv_build_batch_info(bi, dl, da, w.s, dr, ds, max_chunk_size=w.max_chunk_size,
-                                 chunk_size_override=chunk_override)
+        if lm_head:
+            B.csgmv_build_lm_head_batch_info(bi, dl, da, w.s, dr, ds, max_chunk_size=w.max_chunk_size)
+        else:
+            B.csgmv_build_batch_info(bi, dl, da, w.s, dr, ds, max_chunk_size=w.max_chunk_size,
+                                     chunk_size_override=chunk_override)
         B.csgmv_qkv(dx, dA, dB, w.offsets, w.c, widest, dy, bi, workspace=ws)
         hy.copy_(dy, non_blocking=True)
 
@@ -486,7 +500,10 @@ def oracle_step(w, rows):
         oracle.embedding(w.ids[rows], w.A_emb, ta[rows], w.ranks)
         return
     chunk = w.chunk_override or oracle.chunk_size(w.s, w.max_chunk_size)
-    oracle.build_batch_info(w.req_lens, w.req_adapter, chunk)
+    if w.meta.get("builder") == "lm_head":
+        oracle.build_lm_head_batch_info(w.req_lens, w.req_adapter, chunk)
+    else:
+        oracle.build_batch_info(w.req_lens, w.req_adapter, chunk)
     ta = oracle.token_adapter(w.req_lens, w.req_adapter)
     oracle.fused(w.x[rows], w.A, w.B, w.offsets, w.c, ta[rows], w.ranks, w.scalings, w.base[rows])
 
@@ -559,8 +576,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=48)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_qkv",
-                    choices=["decode_qkv", "prefill_gate_up", "skewed_down_proj", "lm_head_decode", "tiny",
-                             "embedding"])
+                    choices=["decode_qkv", "prefill_gate_up", "skewed_down_proj", "lm_head_decode", "lm_head_pruned",
+                             "tiny", "embedding"])
     ap.add_argument("--chunk", type=int, default=128, help="chunk size of skewed_down_proj")
     ap.add_argument("--scale", type=float, default=1.0, help="token scale of the prefill workloads")
     ap.add_argument("--bs", type=int, default=0, help="requests of the decode workloads (0 = default)")

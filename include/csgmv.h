@@ -147,6 +147,35 @@ CSGMV_API int csgmv_build_batch_info(csgmv_batch_info *bi, const int32_t *req_le
                            int use_cuda_graph, csgmv_stream_t stream);
 
 /*
+ * Batch info of a pruned lm_head pass (chunked_backend.py
+ * _prepare_lm_head_batch_info and _build_lm_head_batch_info): only
+ * pruned_lens[i] tokens of request i go through lm_head, and they stay in
+ * their original order, so the permutation is the identity.  Segments come
+ * from merge_and_chunk_segments(weight_indices, pruned_lens, chunk), whose
+ * body is not on the pages; read from its call sites: consecutive requests on
+ * the same slot form one run (requests without pruned tokens are skipped, so
+ * runs merge across them), and every run is cut into pieces of chunk tokens,
+ * the last one shorter.  chunk = chunk_size_override if > 0, else
+ * csgmv_chunk_size(num_tokens, max_chunk_size).
+ *   pruned_lens[bs], req_adapter[bs]   device; pruned tokens and slot of each
+ *                                      request, in request order
+ *   num_tokens                         host; sum of pruned_lens
+ *   lora_ranks, scalings, num_loras, use_cuda_graph   as csgmv_build_batch_info
+ * The result drives csgmv_shrink / csgmv_expand / csgmv_qkv over the pruned
+ * rows (x and base_output with num_tokens rows).  Runs here follow request
+ * order, not slot order, so the batch info needs max_segments of up to
+ * ceil(num_tokens / chunk) plus the number of requests with pruned tokens
+ * (CSGMV_STATUS_CAPACITY otherwise).  req_seg_indptr and
+ * req_weight_indices are not written.  One single-CTA kernel; errors as
+ * csgmv_build_batch_info.
+ */
+CSGMV_API int csgmv_build_lm_head_batch_info(csgmv_batch_info *bi, const int32_t *pruned_lens,
+                                   const int32_t *req_adapter, int bs, int num_tokens,
+                                   const int32_t *lora_ranks, const float *scalings, int num_loras,
+                                   int max_chunk_size, int chunk_size_override, int use_cuda_graph,
+                                   csgmv_stream_t stream);
+
+/*
  * Shrink (base_backend.py run_lora_a_sgemm; chunked_backend.py
  * run_lora_a_sgemm with num_slices): for token t on slot w with rank r,
  *     h[t][j*r + k] = sum_i x[t][i] * A[w][j*r + k][i]     (j < c, k < r)

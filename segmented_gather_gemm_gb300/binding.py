@@ -22,7 +22,7 @@ STATUS_BITS = {
 }
 
 EXPORTED = ["csgmv_last_error", "csgmv_version", "csgmv_chunk_size", "csgmv_batch_info_capacity",
-            "csgmv_build_batch_info", "csgmv_shrink", "csgmv_expand", "csgmv_qkv", "csgmv_qkv_workspace_bytes",
+            "csgmv_build_batch_info", "csgmv_build_lm_head_batch_info", "csgmv_shrink", "csgmv_expand", "csgmv_qkv", "csgmv_qkv_workspace_bytes",
             "csgmv_qkv_static_scratch", "embedding_lora_a"]
 
 
@@ -62,6 +62,7 @@ def lib():
         "csgmv_chunk_size": (i32, [i32, i32]),
         "csgmv_batch_info_capacity": (i32, [i32, i32, i32p, i32p]),
         "csgmv_build_batch_info": (i32, [bip, vp, vp, i32, i32, vp, vp, i32, i32, i32, i32, vp]),
+        "csgmv_build_lm_head_batch_info": (i32, [bip, vp, vp, i32, i32, vp, vp, i32, i32, i32, i32, vp]),
         "csgmv_shrink": (i32, [vp, i64, i64, vp, i32, vp, i32, i64, bip, vp]),
         "csgmv_expand": (i32, [vp, i32, i64, vp, i64, i32p, i32, i32, vp, i32, bip, vp]),
         "csgmv_qkv": (i32, [vp, i64, vp, vp, i64, i32p, i32, i32, vp, vp, ctypes.c_size_t, bip, vp]),
@@ -175,6 +176,18 @@ def csgmv_build_batch_info(bi: BatchInfo, req_lens: torch.Tensor, req_adapter: t
                                         int(num_tokens), _ptr(lora_ranks), _ptr(scalings),
                                         int(lora_ranks.numel()), int(max_chunk_size),
                                         int(chunk_size_override), int(bool(use_cuda_graph)), _stream(stream)))
+
+
+def csgmv_build_lm_head_batch_info(bi: BatchInfo, pruned_lens: torch.Tensor, req_adapter: torch.Tensor,
+                                   num_tokens: int, lora_ranks: torch.Tensor, scalings: torch.Tensor,
+                                   max_chunk_size: int = 128, chunk_size_override: int = 0,
+                                   use_cuda_graph: bool = False, stream=None) -> None:
+    bs = int(pruned_lens.numel())
+    _check(lib().csgmv_build_lm_head_batch_info(ctypes.byref(bi.c), _ptr(pruned_lens), _ptr(req_adapter), bs,
+                                                int(num_tokens), _ptr(lora_ranks), _ptr(scalings),
+                                                int(lora_ranks.numel()), int(max_chunk_size),
+                                                int(chunk_size_override), int(bool(use_cuda_graph)),
+                                                _stream(stream)))
 
 
 def csgmv_shrink(x: torch.Tensor, A: torch.Tensor, num_slices: int, h: torch.Tensor, bi: BatchInfo,

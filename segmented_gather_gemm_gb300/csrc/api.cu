@@ -180,6 +180,47 @@ int csgmv_build_batch_info(csgmv_batch_info *bi, const int32_t *req_lens, const 
     return CSGMV_OK;
 }
 
+int csgmv_build_lm_head_batch_info(csgmv_batch_info *bi, const int32_t *pruned_lens, const int32_t *req_adapter,
+                                   int bs, int num_tokens, const int32_t *lora_ranks, const float *scalings,
+                                   int num_loras, int max_chunk_size, int chunk_size_override, int use_cuda_graph,
+                                   csgmv_stream_t stream) {
+    int rc = check_bi(bi, false);
+    if (rc) return rc;
+    if (bs < 0 || num_tokens < 0 || num_loras < 0)
+        return fail(CSGMV_ERR_INVALID_ARG, "negative bs / num_tokens / num_loras");
+    if (bs > 0 && (!pruned_lens || !req_adapter))
+        return fail(CSGMV_ERR_INVALID_ARG, "pruned_lens / req_adapter is NULL");
+    if (num_loras > 0 && (!lora_ranks || !scalings))
+        return fail(CSGMV_ERR_INVALID_ARG, "lora_ranks / scalings is NULL");
+    if (bs > bi->max_bs) return fail(CSGMV_ERR_CAPACITY, "bs %d exceeds max_bs %d", bs, bi->max_bs);
+    if (num_tokens > bi->max_tokens)
+        return fail(CSGMV_ERR_CAPACITY, "num_tokens %d exceeds max_tokens %d", num_tokens, bi->max_tokens);
+    if (num_loras > bi->max_loras)
+        return fail(CSGMV_ERR_CAPACITY, "num_loras %d exceeds max_loras %d", num_loras, bi->max_loras);
+    if (chunk_size_override < 0) return fail(CSGMV_ERR_INVALID_ARG, "negative chunk_size_override");
+    if (csgmv::build_lm_head_smem_bytes(bs) > 227 * 1024)
+        return fail(CSGMV_ERR_UNSUPPORTED, "bs %d exceeds the single-CTA builder", bs);
+    const int chunk = chunk_size_override > 0 ? chunk_size_override : csgmv_chunk_size(num_tokens, max_chunk_size);
+    csgmv::BuildParams p;
+    p.req_lens = pruned_lens;
+    p.req_adapter = req_adapter;
+    p.ranks_in = lora_ranks;
+    p.scalings_in = scalings;
+    p.bs = bs;
+    p.num_tokens = num_tokens;
+    p.num_loras = num_loras;
+    p.chunk = chunk;
+    p.use_graph = use_cuda_graph ? 1 : 0;
+    cudaError_t e = csgmv::launch_build_lm_head(p, *bi, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "csgmv_build_lm_head_batch_info launch");
+    bi->num_tokens = num_tokens;
+    bi->chunk_size = chunk;
+    bi->bs = bs;
+    bi->num_loras = num_loras;
+    bi->use_cuda_graph = p.use_graph;
+    return CSGMV_OK;
+}
+
 int csgmv_shrink(const void *x, int64_t s, int64_t K, const void *A, int num_slices, void *h, int h_dtype,
                  int64_t ldh, const csgmv_batch_info *bi, csgmv_stream_t stream) {
     int rc = check_bi(bi, true);

@@ -273,7 +273,158 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
     }
 }
 
+// Inclusive block-wide maximum scan of v; the block maximum goes to *total.
+__device__ int block_inclusive_max_scan(int v, int *warp_sums, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc = max(inc, n);
+    }
+    if (lane == 31) warp_sums[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w = max(w, n);
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int r = warp > 0 ? max(warp_sums[warp - 1], inc) : inc;
+    *total = warp_sums[kWarps - 1];
+    __syncthreads();
+    return r;
+}
+
+// Batch info of a pruned lm_head pass (chunked_backend.py
+// _prepare_lm_head_batch_info / _build_lm_head_batch_info): the pruned tokens
+// stay in their original order (identity permutation); a token starts a run
+// when its slot differs from the previous pruned token's, and a segment at
+// every chunk-th token of a run.  Requests without pruned tokens contribute
+// no token, so runs merge across them.  Tiles of 1024 tokens; the current
+// run's start and the segment count carry from tile to tile.
+__global__ void __launch_bounds__(kBuildThreads, 1)
+build_lm_head_kernel(BuildParams p, csgmv_batch_info bi) {
+    extern __shared__ int sm[];
+    const int L = bi.max_loras;
+    int *req_start = sm;                   // [bs+1] first pruned token of request i
+    int *warp_sums = req_start + p.bs + 1;  // [32]
+    int *flags = warp_sums + kWarps;       // [0] error bits
+    const int tid = threadIdx.x;
+    const int chunk = p.chunk;
+    if (tid == 0) flags[0] = 0;
+    __syncthreads();
+
+    // Slot table (lora_manager.py prepare_lora_batch: lora_ranks / scalings per slot).
+    for (int a = tid; a < L; a += kBuildThreads) {
+        int r = 0;
+        float sc = 0.f;
+        if (a < p.num_loras) {
+            r = p.ranks_in[a];
+            sc = p.scalings_in[a];
+            if (r < 0 || r > bi.max_rank) { atomicOr(&flags[0], CSGMV_STATUS_BAD_RANK); r = 0; }
+        }
+        bi.lora_ranks[a] = r;
+        bi.scalings[a] = sc;
+    }
+    // First pruned token of every request, and validation.
+    int carry = 0;
+    for (int i0 = 0; i0 < p.bs; i0 += kBuildThreads) {
+        const int i = i0 + tid;
+        int l = 0;
+        if (i < p.bs) {
+            l = p.req_lens[i];
+            const int a = p.req_adapter[i];
+            if (a < 0 || a >= p.num_loras) atomicOr(&flags[0], CSGMV_STATUS_BAD_ADAPTER);
+            if (l < 0) { atomicOr(&flags[0], CSGMV_STATUS_BAD_LENS); l = 0; }
+        }
+        int tot;
+        const int pre = block_exclusive_scan(l, warp_sums, &tot);
+        if (i < p.bs) req_start[i] = carry + pre;
+        carry += tot;
+    }
+    if (tid == 0) {
+        req_start[p.bs] = carry;
+        if (carry != p.num_tokens) atomicOr(&flags[0], CSGMV_STATUS_BAD_LENS);
+    }
+    __syncthreads();
+    const int err = flags[0];
+    if (err) {
+        if (tid == 0) {
+            *bi.num_segments_dev = 0;
+            *bi.max_len_dev = chunk;
+            bi.seg_indptr[0] = 0;
+            *bi.status = err;
+        }
+        return;
+    }
+
+    const int s = p.num_tokens;
+    auto slot_of = [&](int t) { return p.req_adapter[last_not_greater(req_start, p.bs + 1, t)]; };
+    int run_carry = 0, seg_carry = 0;
+    for (int t0 = 0; t0 < s; t0 += kBuildThreads) {
+        const int t = t0 + tid;
+        const bool valid = t < s;
+        const int a = valid ? slot_of(t) : -1;
+        const bool run_start = valid && (t == 0 || slot_of(t - 1) != a);
+        int rmax;
+        int rs = block_inclusive_max_scan(run_start ? t : -1, warp_sums, &rmax);
+        rs = max(rs, run_carry);
+        const int seg_start = valid && ((t - rs) % chunk == 0);
+        int nnew;
+        const int seg = seg_carry + block_exclusive_scan(seg_start, warp_sums, &nnew);
+        if (seg_start && seg < bi.max_segments) {
+            bi.weight_indices[seg] = a;
+            bi.seg_indptr[seg] = t;
+        }
+        if (valid) bi.permutation[t] = t;
+        run_carry = max(run_carry, rmax);
+        seg_carry += nnew;
+    }
+    const int nseg = seg_carry;
+    if (nseg > bi.max_segments) {
+        if (tid == 0) {
+            *bi.num_segments_dev = 0;
+            *bi.max_len_dev = chunk;
+            bi.seg_indptr[0] = 0;
+            *bi.status = CSGMV_STATUS_CAPACITY;
+        }
+        return;
+    }
+    if (tid == 0) bi.seg_indptr[nseg] = s;
+    if (p.use_graph) {
+        for (int k = nseg + tid; k < bi.max_segments; k += kBuildThreads) {
+            bi.weight_indices[k] = 0;
+            bi.seg_indptr[k + 1] = s;
+        }
+    }
+    if (tid == 0) {
+        *bi.num_segments_dev = nseg;
+        *bi.max_len_dev = chunk;
+        *bi.status = 0;
+    }
+}
+
 }  // namespace
+
+size_t build_lm_head_smem_bytes(int bs) { return sizeof(int) * ((size_t)bs + 1 + kWarps + 2); }
+
+cudaError_t launch_build_lm_head(const BuildParams &p, const csgmv_batch_info &bi, cudaStream_t stream) {
+    size_t smem = build_lm_head_smem_bytes(p.bs);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(build_lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             227 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    build_lm_head_kernel<<<1, kBuildThreads, smem, stream>>>(p, bi);
+    return cudaGetLastError();
+}
 
 size_t build_smem_bytes(int bs, int max_loras) {
     return sizeof(int) * ((size_t)4 * max_loras + 1 + 2 * (size_t)bs + 1 + kWarps + 2 + (size_t)kWarps * max_loras);

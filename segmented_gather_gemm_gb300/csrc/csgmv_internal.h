@@ -68,6 +68,8 @@ struct BuildParams {
 };
 size_t build_smem_bytes(int bs, int max_loras);
 cudaError_t launch_build(const BuildParams &p, const csgmv_batch_info &bi, cudaStream_t stream);
+size_t build_lm_head_smem_bytes(int bs);
+cudaError_t launch_build_lm_head(const BuildParams &p, const csgmv_batch_info &bi, cudaStream_t stream);
 
 // embedding.cu
 struct EmbeddingParams {

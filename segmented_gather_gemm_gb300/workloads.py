@@ -225,6 +225,26 @@ def lm_head_decode(seed: int = 0, bs: int = 512, pad_value=None, with_tensors=Tr
     return _finish(w, rng, 0.02, 0.02, 0.02, 0.02, pad_value, with_tensors)
 
 
+def lm_head_pruned(seed: int = 0, bs: int = 64, pad_value=None, with_tensors=True) -> LoraWorkload:
+    """Pruned lm_head LoRA after a prefill batch: only the last token of each of
+    bs requests reaches lm_head (req_lens holds the pruned token counts, 1 each),
+    in request order; hidden 4096 -> vocab 128256, c = 1, 32 slots of rank 32
+    assigned uniformly, N(0, 0.02), scaling 2.0.  meta["builder"] = "lm_head":
+    the batch info comes from the pruned lm_head builder (identity permutation)."""
+    rng = np.random.default_rng(seed)
+    L = 32
+    lens = np.ones(bs, np.int32)
+    adapter = rng.integers(0, L, size=bs).astype(np.int32)
+    ranks = np.full(L, 32, np.int32)
+    w = LoraWorkload(f"lm_head_pruned_bs{bs}_k4096_n128256_r32",
+                     req_lens=lens, req_adapter=adapter, ranks=ranks,
+                     scalings=np.full(L, 2.0, np.float32),
+                     K=4096, N=128256, c=1, R=32,
+                     offsets=np.array([0, 128256], np.int32),
+                     max_chunk_size=128, chunk_override=0, meta={"builder": "lm_head"})
+    return _finish(w, rng, 0.02, 0.02, 0.02, 0.02, pad_value, with_tensors)
+
+
 def embedding_gather(seed: int = 0, n_req: int = 16, req_len: int = 512, V: int = 128256,
                      R: int = 32, L: int = 32, pad_value=None) -> EmbeddingWorkload:
     """Embedding LoRA-A: n_req requests of req_len tokens, ids uniform in [0, V),
