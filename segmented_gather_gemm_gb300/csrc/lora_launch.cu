@@ -375,10 +375,13 @@ cudaError_t launch_lora_ws(int mode, LoraParams &p, const csgmv_batch_info &bi, 
     k.max_segments = bi.max_segments;
     k.runcap = std::max(1, std::min(bi.max_segments, bi.max_loras + std::max(bi.max_bs, 1)));
     const size_t budget = 227 * 1024;
-    int S1 = 4, S2 = 8;  // S2 even: expand stages go in pairs
+    // S2 even: expand stages go in pairs; a shrink-only launch has no expand
+    // ring, so its shrink ring takes the room
+    int S1 = mode == kModeShrink ? 8 : 4, S2 = 8;
     size_t smem = carve_ws(k, mode, S1, S2);
     while (smem > budget) {
-        if (S2 > 4) S2 -= 2;
+        if (mode == kModeShrink && S1 > 2) --S1;
+        else if (S2 > 4) S2 -= 2;
         else if (S1 > 2) --S1;
         else if (S2 > 2) S2 -= 2;
         else return cudaErrorInvalidConfiguration;
@@ -511,7 +514,7 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
     // depths: decode tiles put every stage of a CTA in flight at once, prefill
     // tiles get as many stages as shared memory holds (up to 8).
     int cs_pick[3] = {0, 0, 0}, res_pick[3] = {0, 0, 0}, s1_pick[3] = {0, 0, 0}, s2_pick[3] = {0, 0, 0};
-    const int cs_list[3] = {8, 4, 2};
+    const int cs_list[3] = {8, 4, 2};  // at most 8: the reduce sums up to eight peers
     const int ncand = mode == kModeExpand ? 1 : 3;
     int best_sms = 0;
     for (int ci = 0; ci < ncand; ++ci) {

@@ -642,19 +642,15 @@ __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int
                     const int row = q * rpr + rr;
                     if (row >= U.M) continue;
                     // every peer's partial is loaded before any is summed, so the
-                    // distributed-shared-memory loads overlap
+                    // distributed-shared-memory loads overlap (clusters of up to 8 CTAs)
+                    float4 t4[8];
+#pragma unroll
+                    for (int peer = 0; peer < 8; ++peer)
+                        if (peer < CS) t4[peer] = dsmem_ld_f4(dsmem_addr(hpart + row * hp + 4 * v, peer));
                     float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int p0 = 0; p0 < CS; p0 += 8) {  // clusters of up to 16 CTAs
-                        float4 t4[8];
 #pragma unroll
-                        for (int jj = 0; jj < 8; ++jj)
-                            if (p0 + jj < CS) t4[jj] = dsmem_ld_f4(dsmem_addr(hpart + row * hp + 4 * v, p0 + jj));
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj)
-                            if (p0 + jj < CS) {
-                                s4.x += t4[jj].x; s4.y += t4[jj].y; s4.z += t4[jj].z; s4.w += t4[jj].w;
-                            }
-                    }
+                    for (int peer = 0; peer < 8; ++peer)
+                        if (peer < CS) { s4.x += t4[peer].x; s4.y += t4[peer].y; s4.z += t4[peer].z; s4.w += t4[peer].w; }
                     *reinterpret_cast<float4 *>(hred + rr * hp + 4 * v) = s4;
                 }
                 cluster_arrive();
