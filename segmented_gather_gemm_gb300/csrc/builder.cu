@@ -58,6 +58,10 @@ __device__ int last_not_greater(const int *a, int n, int key) {
 __global__ void __launch_bounds__(kBuildThreads, 1)
 build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
     extern __shared__ int sm[];
+    // The LoRA kernel that consumes this batch info may start launching now
+    // (programmatic dependent launch); it waits for this kernel to finish
+    // before it reads anything.
+    griddep_launch_dependents();
     const int L = bi.max_loras;
     int *cnt = sm;                      // [L]   tokens per slot
     int *tokbase = cnt + L;             // [L]   first sorted position of slot a
@@ -310,6 +314,7 @@ __device__ int block_inclusive_max_scan(int v, int *warp_sums, int *total) {
 __global__ void __launch_bounds__(kBuildThreads, 1)
 build_lm_head_kernel(BuildParams p, csgmv_batch_info bi) {
     extern __shared__ int sm[];
+    griddep_launch_dependents();  // as in build_batch_info_kernel
     const int L = bi.max_loras;
     int *req_start = sm;                   // [bs+1] first pruned token of request i
     int *warp_sums = req_start + p.bs + 1;  // [32]

@@ -11,6 +11,20 @@ constexpr int kMinChunkSize = 16;  // chunked_backend.py MIN_CHUNK_SIZE
 constexpr int kMaxRank = 64;       // largest buffer rank R the LoRA kernels take
 constexpr int kMaxSlices = 3;
 
+#ifdef __CUDACC__
+// Programmatic dependent launch.  A kernel launched with
+// cudaLaunchAttributeProgrammaticStreamSerialization may start while the
+// kernel before it in the stream is still running; it calls griddep_wait()
+// before its first access to global memory, which returns once that kernel
+// has finished and its writes are visible (at once after a normal launch).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Lets a kernel launched next with that attribute start launching now; it
+// still waits for this kernel's completion in griddep_wait().
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+#endif
+
 enum LoraMode { kModeFused = 0, kModeShrink = 1, kModeExpand = 2 };
 
 // Everything one launch of the shrink / expand / fused kernel needs.  Batch

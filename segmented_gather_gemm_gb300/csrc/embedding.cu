@@ -22,6 +22,7 @@ embedding_lora_a_kernel(EmbeddingParams p, const int32_t *__restrict__ seg_indpt
                         const int32_t *__restrict__ weight_indices, const int32_t *__restrict__ permutation,
                         const int32_t *__restrict__ ranks, const int32_t *__restrict__ nseg_dev,
                         int32_t *status) {
+    griddep_wait();  // the batch info may come from the kernel launched just before
     const int nseg = *nseg_dev;
     const int ty = threadIdx.x >> 5, tx = threadIdx.x & 31;
     for (int seg = blockIdx.x; seg < nseg; seg += gridDim.x) {
@@ -87,9 +88,23 @@ cudaError_t launch_embedding(const EmbeddingParams &p, const csgmv_batch_info &b
     gy = gy < 1 ? 1 : (gy > 64 ? 64 : gy);
     const int gx = bi.max_segments < 1 ? 1 : bi.max_segments;
     dim3 grid(gx, gy, 1);
-    embedding_lora_a_kernel<<<grid, kEmbThreads, 0, stream>>>(p, bi.seg_indptr, bi.weight_indices,
-                                                             bi.permutation, bi.lora_ranks,
-                                                             bi.num_segments_dev, bi.status);
+    // programmatic dependent launch: the blocks start while the batch-info
+    // builder before it finishes, and wait for it on the device
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kEmbThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, embedding_lora_a_kernel, p, (const int32_t *)bi.seg_indptr,
+                                       (const int32_t *)bi.weight_indices, (const int32_t *)bi.permutation,
+                                       (const int32_t *)bi.lora_ranks, (const int32_t *)bi.num_segments_dev,
+                                       (int32_t *)bi.status);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

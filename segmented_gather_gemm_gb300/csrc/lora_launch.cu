@@ -64,6 +64,15 @@ cudaError_t ensure_attrs(const void *fn, int dev, int cluster) {
     return cudaSuccess;
 }
 
+// Programmatic dependent launch: the kernel's CTAs may launch and set up
+// their barriers while the kernel before it in the stream (typically the
+// batch-info builder, which allows it at its start) is still running; every
+// LoRA kernel waits for that kernel on the device before reading global memory.
+void set_dependent_launch(cudaLaunchAttribute *a) {
+    a->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a->val.programmaticStreamSerializationAllowed = 1;
+}
+
 // Co-resident clusters of `cluster` CTAs (or CTAs when cluster == 1).
 cudaError_t resident(const void *fn, int dev, int cluster, size_t smem, int *out, int threads = kTmaThreads) {
     {
@@ -341,13 +350,14 @@ cudaError_t launch_lora_small(int mode, LoraParams &p, const csgmv_batch_info &b
     cfg.blockDim = dim3(kConsumerThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    set_dependent_launch(&attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (info) {
         info->tm = tm;
         info->crmax = rmax;
@@ -438,8 +448,10 @@ cudaError_t launch_lora_ws(int mode, LoraParams &p, const csgmv_batch_info &bi, 
     cfg.blockDim = dim3(kWsThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
+    cudaLaunchAttribute attr[1];
+    set_dependent_launch(&attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (info) {
         info->tm = 128;
         info->crmax = rmax;
@@ -611,13 +623,14 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
     cfg.blockDim = dim3(kTmaThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    set_dependent_launch(&attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (info) {
         info->tm = tm;
         info->crmax = rmax;

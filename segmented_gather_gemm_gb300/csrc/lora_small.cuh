@@ -67,6 +67,10 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
 
     for (int64_t u = cid; u < nunits; u += ncl) {
         const Unit U = decode_unit<TM>(k, smem, nruns, u);
+        // token-list entry m_tok of this thread (the last warps read the list),
+        // loaded alongside the slot's rank; p0 + m < num_tokens for m < M
+        const int m_tok = kConsumerThreads - 1 - tid;
+        const int t_pre = m_tok < TM && m_tok < U.M ? p.permutation[U.p0 + m_tok] : -1;
         const int r = unit_rank(p, U, q == 0 && tid == 0);
         if (r < 0) continue;
         int nt = 0, n0 = 0, n1 = 0;
@@ -115,17 +119,17 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
                     my_bytes += abox;
                 }
         }
-        // token list, read by the last warps (the first ones are issuing TMA)
-        for (int m = kConsumerThreads - 1 - tid; m >= 0 && m < TM; m += kConsumerThreads) {
+        // token list, written by the last warps (the first ones are issuing TMA)
+        if (m_tok >= 0 && m_tok < TM) {
             int t = -1;
-            if (m < U.M) {
-                t = p.permutation[U.p0 + m];
+            if (m_tok < U.M) {
+                t = t_pre;
                 if (t < 0 || t >= p.num_tokens) {
                     atomicOr(p.status, CSGMV_STATUS_BAD_PERMUTATION);
                     t = -1;
                 }
             }
-            tok[m] = t;
+            tok[m_tok] = t;
         }
         __syncthreads();
 

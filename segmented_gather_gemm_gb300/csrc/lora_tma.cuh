@@ -145,6 +145,7 @@ __device__ int build_run_table(const TmaKernelParams &k, unsigned char *smem, in
     int *run_tp = run_w + k.runcap;        // [runcap + 1]
     int *scratch = run_tp + k.runcap + 1;  // [32]
     const int tid = threadIdx.x, nt = blockDim.x;
+    griddep_wait();  // the batch info may come from the kernel launched just before
     // Every word a thread needs is loaded in one round, bounded by the
     // capacity rather than by the segment count (which is loaded alongside).
     const int cap = k.max_segments;

@@ -540,6 +540,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) lora_ws_kernel(const __grid_con
     // The carve-up assumes the dynamic window starts on a 1024-byte boundary
     // (no slack is reserved); refuse to run otherwise.
     if (smem != smem_raw) {
+        griddep_wait();
         if (threadIdx.x == 0) atomicOr(k.p.status, kStatusTimeout);
         return;
     }
