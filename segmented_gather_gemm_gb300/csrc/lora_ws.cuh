@@ -140,6 +140,8 @@ __device__ void ws_producer(const TmaKernelParams &k, unsigned char *smem, int n
         }
         const int t0 = tok[0];
         const bool contig = W.flag[tb] != 0;
+        const int tfill = t0 >= 0 ? t0 : 0;
+        auto grow = [&](int m) { return m < U.M && tok[m] >= 0 ? tok[m] : tfill; };
         ++uc;
 
         if (STREAM == 0 && MODE != kModeExpand) {
@@ -149,19 +151,17 @@ __device__ void ws_producer(const TmaKernelParams &k, unsigned char *smem, int n
                 unsigned char *xs = smem + k.o_sh + s * k.sh_stage;
                 const int k0 = ci * 64;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&W.sh_full[s], k.a_rows * 128 + (contig ? 128 * 128 : 0));
+                    mbar_arrive_expect_tx(&W.sh_full[s], k.a_rows * 128 + 128 * 128);
                     tma_load_2d(xs + k.sh_a, &k.tmA, k0, U.w * cR, &W.sh_full[s]);
                     if (contig) tma_load_2d(xs, &k.tmX, k0, t0, &W.sh_full[s]);
                 }
                 if (!contig) {
-                    for (int idx = lane; idx < U.M * 8; idx += 32) {
-                        const int m = idx >> 3, ch = idx & 7;
-                        const int t = tok[m];
-                        const int64_t kk = (int64_t)k0 + ch * 8;
-                        const bool ok = t >= 0 && kk < p.K;
-                        cp_async16(xs + m * 128 + ((ch ^ (m & 7)) << 4), ok ? p.x + (int64_t)t * p.K + kk : p.x,
-                                   ok ? 16 : 0);
-                    }
+                    // lane l: rows 4l .. 4l+3 in one TMA gather; rows past the tile
+                    // (and rows of an invalid token) read a valid row, never used
+                    __syncwarp();  // after the byte count is posted
+                    const int m = 4 * lane;
+                    tma_gather4(xs + m * 128, &k.tmXg, k0, grow(m), grow(m + 1), grow(m + 2), grow(m + 3),
+                                &W.sh_full[s]);
                 }
                 cp_async_mbar_arrive(&W.sh_full[s]);
                 ++sh_i;
@@ -569,6 +569,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) lora_ws_kernel(const __grid_con
         prefetch_tmap(&k.tmB);
         prefetch_tmap(&k.tmX);
         prefetch_tmap(&k.tmY);
+        prefetch_tmap(&k.tmXg);
     }
     if (warp == 3) {  // one warp owns the TMEM accumulators of the CTA
         tmem_alloc(W.tmem_slot, kWsTmemCols);
