@@ -51,22 +51,15 @@ bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
     return r == CUDA_SUCCESS;
 }
 
-// One-row boxes of x and base for TMA 4-row gathers (128-token tiles whose
-// tokens are not consecutive); unused ones point at a valid tensor.
+// One-row boxes of x for TMA 4-row gathers (128-token tiles whose tokens are
+// not consecutive); otherwise it points at a valid tensor.
 bool encode_row_gathers(TmaKernelParams &k, int mode, int s) {
     const LoraParams &p = k.p;
-    bool ok = true;
     if (k.row_tma && mode != kModeExpand)
-        ok = ok && encode_2d(&k.tmXg, p.x, (uint64_t)p.K, (uint64_t)s, (uint64_t)p.K * 2, 64, 1,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
-    else
-        k.tmXg = k.tmA;
-    if (k.row_tma && mode != kModeShrink)
-        ok = ok && encode_2d(&k.tmYg, p.y, (uint64_t)p.N, (uint64_t)s, (uint64_t)p.N * 2, 64, 1,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
-    else
-        k.tmYg = k.tmA;
-    return ok;
+        return encode_2d(&k.tmXg, p.x, (uint64_t)p.K, (uint64_t)s, (uint64_t)p.K * 2, 64, 1,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    k.tmXg = k.tmA;
+    return true;
 }
 
 cudaError_t ensure_attrs(const void *fn, int dev, int cluster) {
@@ -360,7 +353,7 @@ cudaError_t launch_lora_small(int mode, LoraParams &p, const csgmv_batch_info &b
                              swizzle_for_row_bytes(p.R * 2));
     if (mode == kModeExpand) k.tmA = k.tmB;
     if (mode == kModeShrink) k.tmB = k.tmA;
-    k.tmX = k.tmY = k.tmXg = k.tmYg = k.tmA;
+    k.tmX = k.tmY = k.tmXg = k.tmA;
     if (!ok) return cudaErrorInvalidValue;
 
     cudaLaunchConfig_t cfg = {};
@@ -635,7 +628,7 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
                              CU_TENSOR_MAP_SWIZZLE_128B);
     else
         k.tmY = k.tmA;
-    ok = ok && encode_row_gathers(k, mode, s);
+    k.tmXg = k.tmA;  // the cluster kernel gathers rows with cp.async
     if (!ok) return cudaErrorInvalidValue;
 
     cudaLaunchConfig_t cfg = {};

@@ -53,9 +53,8 @@ struct TmaKernelParams {
     CUtensorMap tmB;    // B (L*N rows, R):   box R x NT, swizzle of the R*2-byte row
     CUtensorMap tmX;    // x (s rows, K): box 64 x TM, 128B swizzle (128-token tiles)
     CUtensorMap tmY;    // base / y (s rows, N): box 64 x TM, 128B swizzle (128-token tiles)
-    CUtensorMap tmXg;   // x, box 64 x 1, 128B swizzle: rows of other 128-token tiles, 4 per gather
-    CUtensorMap tmYg;   // base, box 64 x 1, 128B swizzle: likewise
-    int row_tma;        // 1: tmX / tmY / tmXg / tmYg are valid (128-token tiles)
+    CUtensorMap tmXg;   // warp-specialized shrink: x, box 64 x 1, 128B swizzle, for 4-row gathers
+    int row_tma;        // 1: tmX / tmY are valid; tiles of consecutive tokens load rows by TMA
     LoraParams p;
     int S1, S2;        // shrink / expand ring depth
     int runcap;        // slot-run capacity of the run table
@@ -527,13 +526,6 @@ __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int
             for (int m = tid; m < U.M; m += kConsumerThreads) mine = mine && tok[m] == t0 + m;
             rows_tma = __syncthreads_and(mine && t0 >= 0 && k.row_tma) != 0;
         }
-        // Other 128-token tiles load rows by TMA 4-row gathers; rows past the
-        // tile (and rows of an invalid token) read a valid row, never used.
-        auto row_gather = [&]() { return TM == 128 && k.row_tma && !rows_tma; };
-        auto grow = [&](int m) {
-            const int t = m < U.M ? tok[m] : -1;
-            return t >= 0 ? t : max(tok[0], 0);
-        };
         const int cr = p.c * r;
         const int crp = (cr + 7) & ~7;
         const int ksteps = (r + 15) / 16;
@@ -551,18 +543,11 @@ __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int
             __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(smem + k.o_sh + s * k.sh_stage);
             const int64_t k0 = (int64_t)(kc0 + ci) * 64;
             if (tid == 0) {  // the A rows of this chunk: one TMA box (and the x rows: another)
-                mbar_arrive_expect_tx(&B.sh_full[s], k.a_rows * 128 + (rows_tma || row_gather() ? TM * 128 : 0));
+                mbar_arrive_expect_tx(&B.sh_full[s], k.a_rows * 128 + (rows_tma ? TM * 128 : 0));
                 tma_load_2d(smem + k.o_sh + s * k.sh_stage + k.sh_a, &k.tmA, (int)k0, U.w * cR, &B.sh_full[s]);
                 if (rows_tma) tma_load_2d(xs, &k.tmX, (int)k0, tok[0], &B.sh_full[s]);
             }
-            if (row_gather()) {
-                if (tid < 32) {  // lane l: rows 4l .. 4l+3 in one gather
-                    __syncwarp();  // after the byte count is posted
-                    const int m = 4 * tid;
-                    tma_gather4(xs + m * 64, &k.tmXg, (int)k0, grow(m), grow(m + 1), grow(m + 2), grow(m + 3),
-                                &B.sh_full[s]);
-                }
-            } else if (!rows_tma)
+            if (!rows_tma)
             for (int idx = tid; idx < U.M * 8; idx += kConsumerThreads) {
                 const int m = idx >> 3, ch = idx & 7;
                 const int t = tok[m];
@@ -580,24 +565,14 @@ __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int
             unsigned char *ys = smem + k.o_ex + e * k.ex_stage;
             const int x0 = n0 + i * G::NT, x1 = min(n1, x0 + G::NT);
             const bool base_tma = rows_tma && p.accumulate;
-            const bool base_gather = row_gather() && p.accumulate;
             if (tid == 0) {  // the B rows of this column tile: one TMA box (base rows: NB64 more)
-                mbar_arrive_expect_tx(&B.ex_full[e],
-                                      G::NT * p.R * 2 + (base_tma || base_gather ? G::NB64 * TM * 128 : 0));
+                mbar_arrive_expect_tx(&B.ex_full[e], G::NT * p.R * 2 + (base_tma ? G::NB64 * TM * 128 : 0));
                 tma_load_2d(ys + k.ex_b, &k.tmB, 0, U.w * (int)p.N + x0, &B.ex_full[e]);
                 if (base_tma)
                     for (int bx = 0; bx < G::NB64; ++bx)
                         tma_load_2d(ys + bx * TM * 128, &k.tmY, x0 + 64 * bx, tok[0], &B.ex_full[e]);
             }
-            if (base_gather) {
-                if (tid < 32) {  // lane l: rows 4l .. 4l+3 of every 64-column box
-                    __syncwarp();
-                    const int m = 4 * tid;
-                    for (int bx = 0; bx < G::NB64; ++bx)
-                        tma_gather4(ys + bx * TM * 128 + m * 128, &k.tmYg, x0 + 64 * bx, grow(m), grow(m + 1),
-                                    grow(m + 2), grow(m + 3), &B.ex_full[e]);
-                }
-            } else if (p.accumulate && !base_tma) {
+            if (p.accumulate && !base_tma) {
                 for (int idx = tid; idx < U.M * (G::NT / 8); idx += kConsumerThreads) {
                     const int m = idx / (G::NT / 8), c8 = idx % (G::NT / 8);
                     const int col = x0 + 8 * c8;
@@ -877,8 +852,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1) lora_tma_kernel(const __grid_c
         if (k.row_tma) {
             prefetch_tmap(&k.tmX);
             prefetch_tmap(&k.tmY);
-            prefetch_tmap(&k.tmXg);
-            prefetch_tmap(&k.tmYg);
         }
     }
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + k.o_tc + 32);
