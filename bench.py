@@ -65,7 +65,8 @@ def algorithmic(w, chunk: int) -> dict:
     """Bytes and FLOPs the path must move / do for workload w: x rows of tokens
     with a rank > 0, A rows c*r_a*K and B columns N*r_a of every used slot with
     r_a > 0, base read + write of covered columns for those tokens, and the
-    int32 indices the kernel reads.  h costs nothing (kept on chip)."""
+    int32 indices the kernel reads.  h is not counted: the fused kernel keeps it
+    on chip, and the workspace path's fp32 round trip is the implementation's own."""
     if isinstance(w, wl.EmbeddingWorkload):
         rt = token_ranks(w)
         s = w.s
