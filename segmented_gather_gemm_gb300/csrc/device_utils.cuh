@@ -121,13 +121,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     return false;
 }
 
-// L2 prefetch of [ptr, ptr + bytes): both 16-byte aligned.  A hint only: it
-// returns nothing to the thread, and L2 is coherent, so a later load sees the
-// latest data even if a prior kernel was still writing it.
-__device__ __forceinline__ void prefetch_l2_bulk(const void *ptr, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(ptr), "r"(bytes) : "memory");
-}
-
 // TMA: 2D tiled load, 4-row gather, 4-row scatter store.
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar) {
     asm volatile(

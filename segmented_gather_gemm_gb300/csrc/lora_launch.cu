@@ -355,15 +355,6 @@ cudaError_t launch_lora_small(int mode, LoraParams &p, const csgmv_batch_info &b
     if (mode == kModeShrink) k.tmB = k.tmA;
     k.tmX = k.tmY = k.tmXg = k.tmA;
     if (!ok) return cudaErrorInvalidValue;
-    // Every input the launch may read fits in a fraction of L2 (a decode
-    // batch): prefetch it all while the batch info is still being built.
-    {
-        const uint64_t sl = (uint64_t)s, Ll = (uint64_t)L;
-        uint64_t bytes = 0;
-        if (mode != kModeExpand) bytes += Ll * cR * (uint64_t)p.K * 2 + sl * (uint64_t)p.K * 2;
-        if (mode != kModeShrink) bytes += Ll * (uint64_t)p.N * p.R * 2 + (p.accumulate ? sl * (uint64_t)p.N * 2 : 0);
-        k.l2_prefetch = bytes <= (32ull << 20) ? 1 : 0;
-    }
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nclusters * cs, 1, 1);

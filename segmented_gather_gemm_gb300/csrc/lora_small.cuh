@@ -416,17 +416,6 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
     }
 }
 
-// This CTA's share of [base, base + bytes) into L2, in pieces of up to 4 KB
-// (bytes and base are multiples of 16).
-__device__ __forceinline__ void prefetch_share(const void *base, uint64_t bytes) {
-    const uint64_t n16 = bytes >> 4;
-    const uint64_t per = (n16 + gridDim.x - 1) / gridDim.x;
-    const uint64_t e0 = per * blockIdx.x, e1 = per * (blockIdx.x + 1);
-    const uint64_t b0 = (e0 < n16 ? e0 : n16) << 4, b1 = (e1 < n16 ? e1 : n16) << 4;
-    for (uint64_t o = b0 + (uint64_t)threadIdx.x * 4096; o < b1; o += (uint64_t)blockDim.x * 4096)
-        prefetch_l2_bulk(reinterpret_cast<const unsigned char *>(base) + o, (uint32_t)(b1 - o < 4096 ? b1 - o : 4096));
-}
-
 template <int TM, int RMAX, int MODE>
 __global__ void __launch_bounds__(kConsumerThreads, 1) lora_small_kernel(const __grid_constant__ TmaKernelParams k) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -448,20 +437,6 @@ __global__ void __launch_bounds__(kConsumerThreads, 1) lora_small_kernel(const _
         fence_mbar_init();
         prefetch_tmap(&k.tmA);
         prefetch_tmap(&k.tmB);
-    }
-    if (k.l2_prefetch) {
-        // Weights and activations do not depend on the batch info: they head
-        // for L2 while the kernel before (the batch-info builder) still runs.
-        const LoraParams &p = k.p;
-        const uint64_t s = (uint64_t)p.num_tokens, L = (uint64_t)p.max_loras;
-        if constexpr (MODE != kModeExpand) {
-            prefetch_share(p.A, L * p.c * p.R * (uint64_t)p.K * 2);
-            prefetch_share(p.x, s * (uint64_t)p.K * 2);
-        }
-        if constexpr (MODE != kModeShrink) {
-            prefetch_share(p.B, L * (uint64_t)p.N * p.R * 2);
-            if (p.accumulate) prefetch_share(p.y, s * (uint64_t)p.N * 2);
-        }
     }
     int nruns = 0;
     const int ntiles = build_run_table<TM>(k, smem, &nruns);  // ends with __syncthreads

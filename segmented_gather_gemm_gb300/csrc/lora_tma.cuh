@@ -71,7 +71,6 @@ struct TmaKernelParams {
     int xpitch, ypitch;  // small-tile kernel: bytes per staged x row / base row
     int kc_per;          // small-tile kernel: 64-wide K chunks staged per CTA
     int wscr_off;        // small-tile kernel: per-warp epilogue scratch, bytes after o_hpart
-    int l2_prefetch;     // small-tile kernel: prefetch every input into L2 before the batch info is ready
 };
 
 // Tensor-core (tcgen05) expand: 128-token tile x 128-column stage, the fp32
