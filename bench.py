@@ -86,16 +86,24 @@ def algorithmic(w, chunk: int) -> dict:
     return {"bytes": b, "flops": flops, "tokens": w.s, "active": int(act.sum())}
 
 
+WIDE_COLS = 32768  # the library's kWideCols
+
+
 def qkv_kernels(w, bi) -> int:
     """Kernels one csgmv_qkv call launches when given a workspace: two (shrink,
-    expand) where the library takes its two-kernel path (128-token tiles,
-    K <= 4096, R >= 16, slice offsets on 16-column boundaries), else one.
-    Mirrors the library's choice for the gpu_launches count."""
+    expand) where the library takes its two-kernel path, else one.  The path
+    is taken by 16- / 32-token tiles with at least WIDE_COLS output columns,
+    and by 128-token tiles with K <= 4096, R >= 16 and slice offsets on
+    16-column boundaries.  Mirrors the library's choice for the gpu_launches
+    count."""
     if isinstance(w, wl.EmbeddingWorkload):
         return 1
     slots = max(1, min(max(w.bs, 1), w.L))
     tm = 16 if w.s // slots <= 16 else (32 if w.s // slots <= 48 else 128)
-    split = tm == 128 and w.K <= 4096 and w.R >= 16 and all(int(o) % 16 == 0 for o in w.offsets)
+    if tm <= 32:
+        split = int(w.offsets[-1]) - int(w.offsets[0]) >= WIDE_COLS
+    else:
+        split = w.K <= 4096 and w.R >= 16 and all(int(o) % 16 == 0 for o in w.offsets)
     return 2 if split else 1
 
 

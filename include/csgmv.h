@@ -219,9 +219,11 @@ CSGMV_API int csgmv_expand(const void *h, int h_dtype, int64_t ldh, const void *
  *   workspace, workspace_bytes   optional device scratch for h (NULL / 0 for
  *       none).  Without it h never leaves the chip (reduced across a
  *       thread-block cluster in distributed shared memory).  With at least
- *       csgmv_qkv_workspace_bytes() bytes, batches of long per-slot runs and
- *       K <= 4096 (prefill) may instead run the shrink and the expand as two
- *       kernels with fp32 h in the workspace, which is faster there.  Its
+ *       csgmv_qkv_workspace_bytes() bytes, two kinds of call may instead run
+ *       the shrink and the expand as two kernels with fp32 h in the
+ *       workspace, which is faster there: batches of long per-slot runs with
+ *       K <= 4096 (prefill), and short per-slot runs with at least 32768
+ *       output columns (a vocabulary-wide lm_head).  Its
  *       contents on entry do not matter; on return they are unspecified.  It
  *       must be 16-byte aligned and must not overlap any other argument.
  */

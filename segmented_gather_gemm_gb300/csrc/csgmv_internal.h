@@ -10,6 +10,7 @@ namespace csgmv {
 constexpr int kMinChunkSize = 16;  // chunked_backend.py MIN_CHUNK_SIZE
 constexpr int kMaxRank = 64;       // largest buffer rank R the LoRA kernels take
 constexpr int kMaxSlices = 3;
+constexpr int kWideCols = 32768;   // output columns from which 16- / 32-token csgmv_qkv calls split
 
 #ifdef __CUDACC__
 // Programmatic dependent launch.  A kernel launched with

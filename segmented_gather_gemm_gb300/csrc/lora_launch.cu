@@ -335,9 +335,11 @@ cudaError_t launch_lora_small(int mode, LoraParams &p, const csgmv_batch_info &b
     if (mode == kModeShrink) {
         k.p.nsplit = 1;
     } else {
+        // column blocks per tile: enough units for every resident cluster
+        // (counted from the expected tiles), each block at least 4 x 64 columns
         const int nblk = (ncols + 63) / 64;
         const int max_split = std::max(1, nblk / (cs * 4));
-        k.p.nsplit = std::max(1, std::min(best_res / std::max(tiles_ub, 1), max_split));
+        k.p.nsplit = std::max(1, std::min(best_res / std::max(tiles_est, 1), max_split));
     }
     const int64_t units_ub = (int64_t)tiles_ub * k.p.nsplit;
     const int nclusters = (int)std::max<int64_t>(1, std::min<int64_t>(best_res, units_ub));
@@ -486,9 +488,15 @@ int token_tile(const LoraParams &p, const csgmv_batch_info &bi) {
 }
 
 bool qkv_split_pays(const LoraParams &p, const csgmv_batch_info &bi) {
+    const int tm = token_tile(p, bi);
+    // Vocabulary-wide outputs on 16- / 32-token tiles: the fused kernel gives
+    // each tile's columns to one cluster, which leaves SMs idle and makes every
+    // CTA stream tens of thousands of columns; with h in the workspace, the
+    // expand-only launch spreads column blocks of every tile over all SMs.
+    if (tm <= 32) return p.off[p.c] - p.off[0] >= kWideCols;
     // the shrink-only kernel for 128-token tiles and K <= 4096, then the
     // tcgen05 expand: measured faster than the fused kernel on prefill
-    if (token_tile(p, bi) != 128 || p.K > 4096 || p.R < 16) return false;
+    if (tm != 128 || p.K > 4096 || p.R < 16) return false;
     for (int j = 0; j <= p.c; ++j)
         if (p.off[j] % 16) return false;
     return true;

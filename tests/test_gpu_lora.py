@@ -59,6 +59,30 @@ def test_fused_with_workspace_matches_oracle(case):
         assert_close(f64(y), oracle_fused(w, base=base), f"fused+workspace base={base} {case}")
 
 
+# (seed, bs, max_len, K, slices, R, L): short requests on a handful of slots and
+# at least 32768 output columns, so that csgmv_qkv with a workspace runs the
+# 16-token shrink into the workspace and then the expand-only launch
+WIDE = [
+    (12, 40, 1, 256, [33024], 32, 6),
+    (13, 24, 3, 136, [16384, 16400], 8, 5),
+]
+
+
+@pytest.mark.parametrize("case", WIDE, ids=["c1r32", "c2r8"])
+def test_wide_output_split_matches_oracle(case):
+    """Vocabulary-wide outputs on small tiles take the two-kernel path: the
+    oracle's result, with and without base, and bit-identical output with NaN
+    in every padding row and column."""
+    w = make(*case, min_len=1)
+    for base in (True, False):
+        y, bi = run_fused(w, base=base, workspace=True)
+        assert bi.device_status() == 0
+        assert_close(f64(y), oracle_fused(w, base=base), f"wide split base={base} {case}")
+    y0, _ = run_fused(w, workspace=True)
+    y1, _ = run_fused(make(*case, pad=float("nan"), min_len=1), workspace=True)
+    assert np.array_equal(y0, y1), f"padding leaked into the output ({case})"
+
+
 def test_tiny_single_slice_workload():
     w = wl.tiny_single_slice()
     for base in (True, False):
