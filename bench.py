@@ -100,8 +100,6 @@ def qkv_kernels(w, bi) -> int:
         return 1
     slots = max(1, min(max(w.bs, 1), w.L))
     tm = 16 if w.s // slots <= 16 else (32 if w.s // slots <= 48 else 128)
-    if int(w.offsets[-1]) - int(w.offsets[0]) >= WIDE_COLS and tm == 16:
-        tm = 32
     if tm <= 32:
         split = int(w.offsets[-1]) - int(w.offsets[0]) >= WIDE_COLS
     else:

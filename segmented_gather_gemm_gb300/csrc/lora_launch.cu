@@ -484,10 +484,6 @@ cudaError_t launch_lora_ws(int mode, LoraParams &p, const csgmv_batch_info &bi, 
 int token_tile(const LoraParams &p, const csgmv_batch_info &bi) {
     const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
     const int tps = p.num_tokens / slots;  // mean tokens per slot run
-    // Every tile of a vocabulary-wide expand streams the slot's whole B (as
-    // many bytes as 16 base rows): 32-token tiles read it once per slot run
-    // of up to 32 tokens.
-    if (p.off[p.c] - p.off[0] >= kWideCols && tps <= 16) return 32;
     return tps <= 16 ? 16 : (tps <= 48 ? 32 : 128);
 }
 
