@@ -17,11 +17,6 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem, int src
                  "r"(src_bytes)
                  : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
                                             const void *p) {
@@ -121,7 +116,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_
     return false;
 }
 
-// TMA: 2D tiled load, 4-row gather, 4-row scatter store.
+// TMA: 2D tiled load, 4-row gather.
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
@@ -135,14 +130,6 @@ __device__ __forceinline__ void tma_gather4(void *dst, const void *tmap, int x, 
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, "
         "{%2, %3, %4, %5, %6}], [%7];\n" ::"r"(smem_u32(dst)),
         "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void tma_scatter4(const void *tmap, int x, int y0, int y1, int y2, int y3,
-                                             const void *src) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.global.shared::cta.tile::scatter4.bulk_group [%0, {%1, %2, %3, %4, %5}], "
-        "[%6];\n" ::"l"(tmap),
-        "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(src))
         : "memory");
 }
 // 2D tiled store of a shared-memory box (bulk async-group completion).
