@@ -240,6 +240,9 @@ int max_slice_span(const LoraParams &p, int parts) {
 }
 
 // Shared-memory carve-up of the small-tile kernel.
+// Columns per expand stage of the small-tile kernel (SmallGeo::NT).
+int small_stage_cols(int mode, int tm) { return tm == 16 && mode == kModeExpand ? 512 : 256; }
+
 size_t carve_small(TmaKernelParams &k, int mode, int tm, int cs, int S2) {
     const int R = k.p.R;
     const int cR = k.p.c * R;
@@ -262,8 +265,9 @@ size_t carve_small(TmaKernelParams &k, int mode, int tm, int cs, int S2) {
     k.xpitch = 16;
     k.o_sh = k.o_ah = k.o_hred = 0;
     // h partials (shrink) and, right after them, the per-warp epilogue scratch
-    // tiles (expand): 16 rows x (256 / WN) columns each, rows padded by 16 bytes
-    const int wcols = 256 / (kConsumerWarps / (tm / 16));
+    // tiles (expand): 16 rows x (NT / WN) columns each, rows padded by 16 bytes
+    const int nt = small_stage_cols(mode, tm);
+    const int wcols = nt / (kConsumerWarps / (tm / 16));
     k.o_hpart = take((size_t)tm * k.hp * 4 + (size_t)kConsumerWarps * 16 * (wcols * 2 + 16), 16);
     k.wscr_off = (int)align_up((size_t)tm * k.hp * 4, 16);
     if (mode != kModeExpand) {
@@ -276,7 +280,6 @@ size_t carve_small(TmaKernelParams &k, int mode, int tm, int cs, int S2) {
     k.ypitch = 16;
     k.ex_b = k.ex_stage = k.o_ex = 0;
     if (mode != kModeShrink) {
-        const int nt = 256;  // columns per expand stage (Geo<16/32>::NT)
         k.ypitch = nt * 2 + 16;
         k.ex_b = (int)align_up((size_t)tm * k.ypitch, 1024);
         k.ex_stage = (int)align_up((size_t)k.ex_b + (size_t)nt * R * 2, 1024);
@@ -316,7 +319,8 @@ cudaError_t launch_lora_small(int mode, LoraParams &p, const csgmv_batch_info &b
         const int cs = mode == kModeExpand ? 1 : cs_list[ci];
         if (mode == kModeExpand && ci > 0) break;
         if (tm % cs) continue;
-        const int stages = std::max(1, (ncols / cs + 255) / 256);
+        const int nt = small_stage_cols(mode, tm);
+        const int stages = std::max(1, (ncols / cs + nt - 1) / nt);
         int S2 = std::min(8, std::max(2, stages + 1));
         size_t smem = carve_small(k, mode, tm, cs, S2);
         while (smem > budget && S2 > 2) smem = carve_small(k, mode, tm, cs, --S2);

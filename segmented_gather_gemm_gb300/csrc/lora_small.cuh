@@ -39,10 +39,23 @@ __device__ __forceinline__ SmallBars small_bars(const TmaKernelParams &k, unsign
     return r;
 }
 
+// Geometry of the small-tile kernel.  Expand stages are 256 columns wide, and
+// 512 for expand-only launches on 16-token tiles: those stream long column
+// ranges (a vocabulary-wide lm_head), where per-stage fixed costs dominate.
+template <int TM, int MODE>
+struct SmallGeo {
+    static constexpr int WM = TM / 16;
+    static constexpr int WN = kConsumerWarps / WM;
+    static constexpr int NT = (TM == 16 && MODE == kModeExpand) ? 512 : 256;
+    static constexpr int WCOLS = NT / WN;
+    static constexpr int EXT = WCOLS / 8;
+    static constexpr int BBOX = 256;  // rows of one B box (the TMA box limit)
+};
+
 template <int TM, int RMAX, int MODE>
 __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q, int CS, int nruns,
                            int64_t nunits, int cid, int ncl) {
-    using G = Geo<TM>;
+    using G = SmallGeo<TM, MODE>;
     constexpr int SHT = (3 * RMAX / 8 + G::WN - 1) / G::WN;  // shrink n8 tiles per warp (c <= 3)
     constexpr int KS = RMAX / 16;                             // expand k16 steps at most
     const LoraParams &p = k.p;
@@ -165,7 +178,10 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
             if (b_copy) bytes += (uint32_t)G::NT * p.R * 2;
             if (row_copy) bytes += (uint32_t)(x1 - x0) * 2;
             mbar_arrive_expect_tx(&B.ex_full[e], bytes);
-            if (b_copy) tma_load_2d(ys + k.ex_b, &k.tmB, 0, U.w * (int)p.N + x0, &B.ex_full[e]);
+            if (b_copy)
+                for (int bb = 0; bb < G::NT / G::BBOX; ++bb)
+                    tma_load_2d(ys + k.ex_b + bb * G::BBOX * p.R * 2, &k.tmB, 0, U.w * (int)p.N + x0 + bb * G::BBOX,
+                                &B.ex_full[e]);
             if (row_copy)
                 bulk_g2s(ys + my_row * k.ypitch, p.y + (int64_t)t * p.N + x0, (uint32_t)(x1 - x0) * 2, &B.ex_full[e]);
             ++ex_is;
