@@ -18,6 +18,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -124,13 +125,17 @@ def load_peaks():
 
 def kernel_source_hash() -> str:
     """Hash of the sources of the shrink / expand / fused kernels and their
-    launcher (the kernels a recorded traffic figure belongs to)."""
+    launcher (the kernels a recorded traffic figure belongs to), with comments
+    and whitespace removed, so that an edit of a comment keeps the record."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "segmented_gather_gemm_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.startswith("lora_") or f in ("device_utils.cuh", "csgmv_internal.h"):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                text = fh.read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
+            h.update(f.encode() + b"\0" + " ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -15,9 +15,10 @@
 //           memory: each CTA sums its share of the rows and writes the sums
 //           into every CTA's copy of h, so the expand reads h locally (as
 //           bf16 hi + lo fragment pairs);
-//   expand  a ring of 256-column stages: the slot's B rows as one TMA box and
-//           each token's base row piece as one bulk copy; y = base + sigma h
-//           B^T on the tensor cores in place, then 16-byte row stores.
+//   expand  a ring of 256-column stages (512 in expand-only launches on
+//           16-token tiles): the slot's B rows as TMA boxes of up to 256 rows
+//           and each token's base row piece as one bulk copy; y = base +
+//           sigma h B^T on the tensor cores in place, then 16-byte row stores.
 // Every barrier arrival carries the bytes its thread copies (expect-tx), so
 // one wait covers a whole stage.  All waits are bounded.
 #pragma once
