@@ -1,0 +1,75 @@
+"""Host-side logic of bench.py that the JSON line depends on: the kernel count
+per csgmv_qkv call (gpu_launches mirrors the library's two-kernel choice), the
+algorithmic bytes of the decode line, and the source hash that keys the
+recorded DRAM traffic."""
+import os
+import shutil
+
+import pytest
+
+import bench
+from segmented_gather_gemm_gb300 import workloads as wl
+
+
+# shapes only (no tensors drawn)
+SHAPES = {
+    "decode_qkv": lambda: wl.decode_qkv(with_tensors=False),
+    "prefill_gate_up": lambda: wl.prefill_gate_up(with_tensors=False),
+    "skewed_down_proj": lambda: wl.skewed_down_proj(with_tensors=False),
+    "lm_head_decode": lambda: wl.lm_head_decode(with_tensors=False),
+    "lm_head_pruned": lambda: wl.lm_head_pruned(with_tensors=False),
+    "tiny": wl.tiny_single_slice,
+}
+
+
+@pytest.mark.parametrize("name, kernels", [
+    ("decode_qkv", 1),         # 32-token tiles, 6144 columns: one fused kernel
+    ("prefill_gate_up", 2),    # 128-token tiles, K = 4096: shrink into the workspace, then expand
+    ("skewed_down_proj", 1),   # K = 14336 is past the two-kernel path's K <= 4096
+    ("lm_head_decode", 2),     # 16-token tiles, 128256 columns: the vocabulary-wide split
+    ("lm_head_pruned", 2),
+    ("tiny", 1),
+])
+def test_kernels_per_call(name, kernels):
+    assert bench.qkv_kernels(SHAPES[name](), None) == kernels
+
+
+def test_embedding_is_one_kernel():
+    assert bench.qkv_kernels(wl.embedding_gather(n_req=2, req_len=4, V=64), None) == 1
+
+
+def test_wide_split_threshold():
+    """The two-kernel path for small tiles starts at WIDE_COLS output columns."""
+    for cols, kernels in ((bench.WIDE_COLS - 8, 1), (bench.WIDE_COLS, 2)):
+        w = wl.random_lora(3, bs=40, max_len=1, K=64, N_slices=[cols], R=16, L=6, min_len=1)
+        assert bench.qkv_kernels(w, None) == kernels
+
+
+def test_decode_algorithmic_bytes():
+    """x, A and B of the used slots and the base read + write: the decode line's
+    13.1 MB (x 2.1 MB, A 3.1 MB, B 1.6 MB, base 2 x 3.1 MB) and its flops."""
+    w = wl.decode_qkv(with_tensors=False)
+    a = bench.algorithmic(w, 128)
+    used = len(set(int(v) for v in w.req_adapter))
+    x = w.s * w.K * 2
+    A = used * w.c * 16 * w.K * 2
+    B = used * w.N * 16 * 2
+    base = 2 * w.s * w.N * 2
+    assert a["tokens"] == w.s
+    assert abs(a["bytes"] - (x + A + B + base)) < 0.01 * (x + A + B + base)
+    assert a["flops"] == pytest.approx(w.s * 2 * 16 * (w.c * w.K + w.N), rel=1e-9)
+
+
+def test_source_hash_ignores_comments(tmp_path, monkeypatch):
+    """A comment edit keeps the recorded traffic; a code edit drops it."""
+    csrc = os.path.join(bench.ROOT, "segmented_gather_gemm_gb300", "csrc")
+    root = tmp_path / "repo"
+    shutil.copytree(csrc, root / "segmented_gather_gemm_gb300" / "csrc")
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    h0 = bench.kernel_source_hash()
+    f = root / "segmented_gather_gemm_gb300" / "csrc" / "lora_small.cuh"
+    text = f.read_text()
+    f.write_text("// a new comment line\n" + text.replace("#pragma once", "#pragma once  /* note */", 1))
+    assert bench.kernel_source_hash() == h0
+    f.write_text(text.replace("#pragma once", "#pragma once\nconstexpr int kUnused = 1;", 1))
+    assert bench.kernel_source_hash() != h0
