@@ -7,7 +7,8 @@
 // output columns).  The roles run concurrently, linked by mbarriers, and the
 // shrink of the next unit streams while the expand of the current one does:
 //   warp 0      shrink producer: the tile's token list, then x rows and the
-//               slot's A tile per 64-wide K chunk into the shrink ring;
+//               slot's A tile per 64-wide K chunk into the shrink ring (x of a
+//               tile of non-consecutive tokens by TMA 4-row gathers);
 //   warp 1      expand producer: base rows and the slot's B tile per
 //               64-column stage into the expand ring.  Tiles of consecutive
 //               tokens load rows as TMA boxes; others gather rows with
