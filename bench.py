@@ -123,14 +123,26 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the sources of the shrink / expand / fused kernels and their
-    launcher (the kernels a recorded traffic figure belongs to), with comments
-    and whitespace removed, so that an edit of a comment keeps the record."""
+# Sources of the kernels behind each recorded traffic figure, with their
+# launcher and shared headers: the small-tile kernel for decode and lm_head
+# shapes, the warp-specialized shrink and the tcgen05 expand for prefill.
+_SHARED_SOURCES = ("lora_tma.cuh", "lora_launch.cu", "device_utils.cuh", "csgmv_internal.h")
+KERNEL_SOURCES = {
+    "decode_qkv": ("lora_small.cuh", "lora_small.cu") + _SHARED_SOURCES,
+    "lm_head_decode": ("lora_small.cuh", "lora_small.cu") + _SHARED_SOURCES,
+    "prefill_gate_up": ("lora_ws.cuh", "lora_ws.cu", "lora_expand.cu") + _SHARED_SOURCES,
+}
+
+
+def kernel_source_hash(workload: str | None = None) -> str:
+    """Hash of the kernel sources a recorded traffic figure belongs to (those
+    of `workload`, else every LoRA kernel source), with comments and
+    whitespace removed, so that an edit of a comment keeps the record."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "segmented_gather_gemm_gb300", "csrc")
+    wanted = KERNEL_SOURCES.get(workload)
     for f in sorted(os.listdir(csrc)):
-        if f.startswith("lora_") or f in ("device_utils.cuh", "csgmv_internal.h"):
+        if (f in wanted) if wanted else (f.startswith("lora_") or f in ("device_utils.cuh", "csgmv_internal.h")):
             with open(os.path.join(csrc, f), encoding="utf-8") as fh:
                 text = fh.read()
             text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -148,7 +160,7 @@ def recorded_traffic(workload: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(workload):
         return None
     return e.get("bytes_per_launch")
 

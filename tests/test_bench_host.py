@@ -73,3 +73,19 @@ def test_source_hash_ignores_comments(tmp_path, monkeypatch):
     assert bench.kernel_source_hash() == h0
     f.write_text(text.replace("#pragma once", "#pragma once\nconstexpr int kUnused = 1;", 1))
     assert bench.kernel_source_hash() != h0
+
+
+def test_source_hash_is_per_workload(tmp_path, monkeypatch):
+    """A change to the small-tile kernel drops the decode and lm_head records
+    but keeps the prefill one, whose kernels do not include it."""
+    csrc = os.path.join(bench.ROOT, "segmented_gather_gemm_gb300", "csrc")
+    root = tmp_path / "repo"
+    shutil.copytree(csrc, root / "segmented_gather_gemm_gb300" / "csrc")
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    before = {w: bench.kernel_source_hash(w) for w in bench.KERNEL_SOURCES}
+    f = root / "segmented_gather_gemm_gb300" / "csrc" / "lora_small.cuh"
+    f.write_text(f.read_text().replace("#pragma once", "#pragma once\nconstexpr int kUnused = 1;", 1))
+    after = {w: bench.kernel_source_hash(w) for w in bench.KERNEL_SOURCES}
+    assert after["prefill_gate_up"] == before["prefill_gate_up"]
+    assert after["decode_qkv"] != before["decode_qkv"]
+    assert after["lm_head_decode"] != before["lm_head_decode"]
