@@ -166,21 +166,15 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
                          B.x_full);
         }
 
-        // base rows and B rows of expand stage `i` into the next ring slot.
-        // Expand-only launches issue every stage from the last warp alone (lane
-        // m: row m; lane 31: B too), so the other warps never wait for a ring
-        // slot; the fused mode spreads its row copies over every warp.
-        constexpr bool kOneIssuer = MODE == kModeExpand;
-        const bool issuer = !kOneIssuer || warp == kConsumerWarps - 1;
-        const int is_row = kOneIssuer ? (lane < TM ? lane : -1) : my_row;
+        // base rows and B rows of expand stage `i` into the next ring slot
         auto issue_stage = [&](int i) {
             const int e = ex_is % k.S2;
             mbar_wait(&B.ex_empty[e], ((ex_is / k.S2) & 1) ^ 1, p.status, kStatusTimeout);
             unsigned char *ys = smem + k.o_ex + e * k.ex_stage;
             const int x0 = n0 + i * G::NT, x1 = min(n1, x0 + G::NT);
-            const int t = is_row >= 0 && is_row < U.M ? tok[is_row] : -1;
+            const int t = my_row >= 0 && my_row < U.M ? tok[my_row] : -1;
             const bool row_copy = t >= 0 && p.accumulate;
-            const bool b_copy = tid == kConsumerThreads - 1;  // the last warp's last lane
+            const bool b_copy = tid == kConsumerThreads - 1;  // a lane of its own: the last warp's last
             uint32_t bytes = 0;
             if (b_copy) bytes += (uint32_t)G::NT * p.R * 2;
             if (row_copy) bytes += (uint32_t)(x1 - x0) * 2;
@@ -190,12 +184,11 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
                     tma_load_2d(ys + k.ex_b + bb * G::BBOX * p.R * 2, &k.tmB, 0, U.w * (int)p.N + x0 + bb * G::BBOX,
                                 &B.ex_full[e]);
             if (row_copy)
-                bulk_g2s(ys + is_row * k.ypitch, p.y + (int64_t)t * p.N + x0, (uint32_t)(x1 - x0) * 2, &B.ex_full[e]);
+                bulk_g2s(ys + my_row * k.ypitch, p.y + (int64_t)t * p.N + x0, (uint32_t)(x1 - x0) * 2, &B.ex_full[e]);
             ++ex_is;
         };
         const int ex_pre = min(nt, k.S2 - 1);
-        if (issuer)
-            for (int i = 0; i < ex_pre; ++i) issue_stage(i);
+        for (int i = 0; i < ex_pre; ++i) issue_stage(i);
 
         if constexpr (MODE != kModeExpand) {
             // ---------------------------------------------------------------- shrink
@@ -333,7 +326,7 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
                 if (wc < min(n1, n0 + G::NT)) load_slice(slice_at(p, wc));
             }
             for (int i = 0; i < nt; ++i) {
-                if (issuer && i + k.S2 - 1 < nt) issue_stage(i + k.S2 - 1);
+                if (i + k.S2 - 1 < nt) issue_stage(i + k.S2 - 1);
                 const int e = ex_it % k.S2;
                 mbar_wait(&B.ex_full[e], (ex_it / k.S2) & 1, p.status, kStatusTimeout);
                 unsigned char *ys = smem + k.o_ex + e * k.ex_stage;
@@ -455,7 +448,7 @@ __global__ void __launch_bounds__(kConsumerThreads, 1) lora_small_kernel(const _
         const SmallBars B = small_bars(k, smem);
         mbar_init(B.x_full, kConsumerThreads);
         for (int i = 0; i < k.S2; ++i) {
-            mbar_init(&B.ex_full[i], MODE == kModeExpand ? 32 : kConsumerThreads);  // every issuing thread
+            mbar_init(&B.ex_full[i], kConsumerThreads);
             mbar_init(&B.ex_empty[i], kConsumerWarps);
         }
         fence_mbar_init();
