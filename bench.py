@@ -2,12 +2,19 @@
 """Benchmark of the csgmv LoRA path on GB300.
 
 One step = one pass of the whole path over one batch: the device batch builder
-(chunk size, stable token permutation, segments) followed by the fused
-shrink->expand kernel (csgmv_qkv).  The default workload is Llama-3-8B-shaped
-decode QKV: 256 requests x 1 token, K = 4096, q/k/v = 4096/1024/1024, c = 3,
-8 slots of rank 16.  Its inputs (13 MB) fit in L2, so steps rotate over enough
-independent input sets (own x, A, B, base and batch) that the set a step
-touches was evicted since it was last used.
+(chunk size, stable token permutation, segments) followed by the
+shrink->expand call (csgmv_qkv, given an h workspace as a caller would).  The
+default workload is the largest configuration that fits one GPU: prefill
+gate_up, 32 requests of U[64, 2048] tokens (~33.8k tokens), K = 4096,
+c = 2 slices of 14336 columns, 16 slots with ranks from {8, 16, 32, 64} on a
+Zipf(1.1) assignment.  Steps rotate over enough independent input sets (own
+x, A, B, base and batch) that the data a step touches is not in L2.
+
+Besides the headline line, every other configuration is measured in the same
+run under `per_config` (CUDA-event time of the csgmv_qkv or embedding call
+and of the builder, its roofline fraction and tokens/s): tiny, decode QKV,
+skewed down_proj at chunk 16 / 32 / 64 / 128, lm_head decode, pruned lm_head
+and the embedding gather.
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead,
 on bounded token samples of the same workload.
@@ -35,6 +42,21 @@ from segmented_gather_gemm_gb300 import workloads as wl  # noqa: E402
 METRIC = "csgmv shrink+expand tokens/s at 1 GB300; % of HBM/tensor roofline vs CPU oracle"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# The configurations measured next to the headline workload: (label, workload,
+# chunk override), and the roofline fraction each one is held to.
+PER_CONFIG = [
+    ("tiny", "tiny", 0),
+    ("decode_qkv", "decode_qkv", 0),
+    ("skewed_down_proj_chunk16", "skewed_down_proj", 16),
+    ("skewed_down_proj_chunk32", "skewed_down_proj", 32),
+    ("skewed_down_proj_chunk64", "skewed_down_proj", 64),
+    ("skewed_down_proj_chunk128", "skewed_down_proj", 128),
+    ("lm_head_decode", "lm_head_decode", 0),
+    ("lm_head_pruned", "lm_head_pruned", 0),
+    ("embedding", "embedding", 0),
+]
+TARGET_FRAC = {"prefill_gate_up": 0.70, "skewed_down_proj": 0.70, "decode_qkv": 0.60, "lm_head_decode": 0.60}
 
 
 # --------------------------------------------------------------------------- workloads
@@ -223,9 +245,11 @@ class ClockSampler:
 # --------------------------------------------------------------------------- GPU arm
 
 class DeviceSet:
-    """One independent input set resident in HBM, with its own batch info."""
+    """One independent input set resident in HBM, with its own batch info.
+    `share` reuses another set's device tensors (same data, another chunk
+    size)."""
 
-    def __init__(self, w, chunk_override: int, max_rank: int):
+    def __init__(self, w, chunk_override: int, max_rank: int, share: "DeviceSet | None" = None):
         import torch
 
         from segmented_gather_gemm_gb300 import binding as B
@@ -239,21 +263,24 @@ class DeviceSet:
         self.ranks = torch.from_numpy(w.ranks).cuda()
         if isinstance(w, wl.EmbeddingWorkload):
             self.scal = torch.ones(w.L, dtype=torch.float32, device="cuda")
-            self.ids = torch.from_numpy(w.ids).cuda()
-            self.A = bf(w.A_emb)
+            self.ids = share.ids if share else torch.from_numpy(w.ids).cuda()
+            self.A = share.A if share else bf(w.A_emb)
             self.out = torch.zeros((w.s, w.R), dtype=torch.bfloat16, device="cuda")
             self.bi = B.BatchInfo.for_batch(len(w.req_lens), w.s, w.L, w.R)
         else:
             self.scal = torch.from_numpy(w.scalings).cuda()
-            self.x, self.A, self.B, self.y = bf(w.x), bf(w.A), bf(w.B), bf(w.base)
+            if share:
+                self.x, self.A, self.B, self.y = share.x, share.A, share.B, share.y
+            else:
+                self.x, self.A, self.B, self.y = bf(w.x), bf(w.A), bf(w.B), bf(w.base)
             if w.meta.get("builder") == "lm_head":  # runs in request order: room for one segment per token
                 self.bi = B.BatchInfo(w.bs, w.s, w.s + 1, max_loras=w.L, max_rank=w.R)
             else:
                 self.bi = B.BatchInfo.for_batch(w.bs, w.s, w.L, w.R, min_chunk=min(16, chunk_override or 16))
             self.widest = int(np.max(np.diff(w.offsets)))
             # h workspace: csgmv_qkv takes its two-kernel path where that is faster
-            self.ws = torch.empty(B.csgmv_qkv_workspace_bytes(self.bi, w.c) // 4, dtype=torch.float32,
-                                  device="cuda")
+            self.ws = share.ws if share else torch.empty(B.csgmv_qkv_workspace_bytes(self.bi, w.c) // 4,
+                                                         dtype=torch.float32, device="cuda")
         self.chunk_override = chunk_override
 
     def build(self):
@@ -333,6 +360,80 @@ def whole_job_rate(world: int, steps: int, tokens_per_step: float, elapsed: floa
     return world * steps * tokens_per_step / elapsed
 
 
+def sets_needed(per_set: int) -> int:
+    """Input sets to rotate so that a step never finds its data in L2: one
+    set when a set alone is over twice the L2, else enough sets to exceed it."""
+    if per_set >= 2 * L2_BYTES:
+        return 1
+    return -(-2 * L2_BYTES // per_set) + 1
+
+
+def roofline_of(alg: dict, seconds: float, peaks: dict) -> dict:
+    """Achieved bytes (or flops) per second of one call against the measured
+    peak, on whichever of HBM bytes or tensor flops bounds the call."""
+    hbm = float(peaks["hbm_gbs"])
+    tc = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    t_hbm = alg["bytes"] / (hbm * 1e9)
+    t_tc = alg["flops"] / (tc * 1e12)
+    if t_hbm >= t_tc:
+        ach = alg["bytes"] / seconds / 1e9
+        r = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4)}
+    else:
+        ach = alg["flops"] / seconds / 1e12
+        r = {"bound": "tensor", "achieved": round(ach, 2), "peak": tc, "unit": "TFLOP/s", "frac": round(ach / tc, 4)}
+    r["roofline_us"] = round(max(t_hbm, t_tc) * 1e6, 3)
+    return r
+
+
+def time_kind(torch, sets, kind: str, target_s: float = 0.05, cap: int = 2400):
+    """Average CUDA-event seconds of one `kind` call ("compute" or "build"),
+    replayed from graphs that rotate over the sets for about target_s."""
+    n0 = len(sets)
+    probe = timed_graphs(torch, sets, n0, kind)
+    time_plan(torch, probe)
+    est = time_plan(torch, probe) / n0
+    reps = int(min(cap, max(n0, target_s / max(est, 1e-7))))
+    reps = -(-reps // n0) * n0
+    plan = timed_graphs(torch, sets, reps, kind)
+    time_plan(torch, plan[:1])
+    return time_plan(torch, plan) / reps, reps
+
+
+def measure_config(torch, label: str, workload: str, chunk: int, peaks: dict, scale: float = 1.0) -> dict:
+    """One configuration on its own input sets: the csgmv_qkv (or embedding)
+    call and the builder, each timed with CUDA events over graph replays, the
+    call's roofline fraction and its tokens/s."""
+    w0 = make_workload(workload, 0, chunk or 128, scale)
+    nsets = sets_needed(set_bytes(w0))
+    ws = [w0] + [make_workload(workload, s, chunk or 128, scale) for s in range(1, nsets)]
+    sets = [DeviceSet(w, chunk, w.R) for w in ws]
+    for s in sets:
+        s.step()
+    torch.cuda.synchronize()
+    status = [s.bi.device_status() for s in sets]
+    if any(status):
+        raise SystemExit(f"{label}: device status {status}")
+    t_call, reps = time_kind(torch, sets, "compute")
+    t_build, _ = time_kind(torch, sets, "build")
+    chunk_used = sets[0].bi.chunk_size
+    algs = [algorithmic(w, chunk_used) for w in ws]
+    alg = {k: float(np.mean([a[k] for a in algs])) for k in ("bytes", "flops", "tokens")}
+    r = roofline_of(alg, t_call, peaks)
+    out = {
+        "workload": w0.name, "call_us": round(t_call * 1e6, 3), "build_us": round(t_build * 1e6, 3),
+        "tokens": alg["tokens"], "tokens_per_s": round(alg["tokens"] / t_call, 1),
+        "step_tokens_per_s": round(alg["tokens"] / (t_call + t_build), 1),
+        "algorithmic_bytes": int(alg["bytes"]), "algorithmic_flops": int(alg["flops"]),
+        "kernels_per_call": qkv_kernels(w0, sets[0].bi), "chunk_size": chunk_used,
+        "input_sets": nsets, "timed_calls": reps,
+    }
+    out.update({k: r[k] for k in ("bound", "achieved", "unit", "frac", "roofline_us")})
+    out["target_frac"] = TARGET_FRAC.get(workload)
+    del sets
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     import torch
 
@@ -353,7 +454,7 @@ def run_gpu(args):
 
     w0 = make_workload(args.workload, 0, args.chunk, args.scale, args.bs)
     per_set = set_bytes(w0)
-    nsets = args.sets or max(1, -(-2 * L2_BYTES // per_set) + 1)
+    nsets = args.sets or sets_needed(per_set)
     seeds = [1000 * rank + i for i in range(nsets)]
     ws = [w0 if s == 0 else make_workload(args.workload, s, args.chunk, args.scale, args.bs) for s in seeds]
     chunk_override = args.chunk if args.workload == "skewed_down_proj" else 0
@@ -371,61 +472,53 @@ def run_gpu(args):
         raise SystemExit(f"device status {status}")
 
     plan = timed_graphs(torch, sets, args.steps, "step")
-    kplan = timed_graphs(torch, sets, min(args.steps, 2400) if args.steps >= nsets else nsets, "compute")
-    bplan = timed_graphs(torch, sets, min(args.steps, 2400) if args.steps >= nsets else nsets, "build")
     time_plan(torch, plan[:1])  # graph upload / first replay
 
     with ClockSampler(local) as clk:
-        # keep the GPU busy on the same steps for ~1 s so the clock samples
+        # keep the GPU busy on the same steps for a while so the clock samples
         # describe this workload, then the timed region
         t_end = time.time() + args.soak_seconds
         while time.time() < t_end:
             time_plan(torch, plan[:1])
         elapsed = time_plan(torch, plan, dist)
     clocks = clk.summary()
-
-    k_steps = sum(1 for _ in range(args.steps))
-    k_compute = min(args.steps, 2400) if args.steps >= nsets else nsets
-    t_compute = time_plan(torch, kplan) / k_compute
-    t_build = time_plan(torch, bplan) / k_compute
-
     if dist is not None:
         elapsed = max_over_ranks(elapsed, dist, "cuda")
 
+    peaks, peak_src = load_peaks()
+    t_compute, k_compute = time_kind(torch, sets, "compute")
+    t_build, _ = time_kind(torch, sets, "build")
+
+    k_steps = args.steps
     chunk = sets[0].bi.chunk_size
     algs = [algorithmic(w, chunk) for w in ws]
     tokens_per_step = float(np.mean([a["tokens"] for a in algs]))
-    bytes_per = float(np.mean([a["bytes"] for a in algs]))
-    flops_per = float(np.mean([a["flops"] for a in algs]))
+    alg = {k: float(np.mean([a[k] for a in algs])) for k in ("bytes", "flops", "tokens")}
     value = whole_job_rate(world, k_steps, tokens_per_step, elapsed)
+
+    breakdown = {"build_batch_info": round(t_build * 1e6, 3), "csgmv_qkv": round(t_compute * 1e6, 3),
+                 "step": round(elapsed / k_steps * 1e6, 3)}
+    kernels = qkv_kernels(w0, sets[0].bi)
+    if kernels == 2 and not isinstance(w0, wl.EmbeddingWorkload):
+        breakdown.update(time_split_kernels(torch, sets))
 
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(torch, ws[0], chunk_override, min(args.steps, 200), world)
+    del sets
+    torch.cuda.empty_cache()
 
-    peaks, peak_src = load_peaks()
-    hbm = float(peaks["hbm_gbs"])
-    tc = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    achieved_gbs = bytes_per / t_compute / 1e9
-    t_hbm = bytes_per / (hbm * 1e9)
-    t_tc = flops_per / (tc * 1e12)
-    bound = "hbm" if t_hbm >= t_tc else "tensor"
-    if bound == "hbm":
-        roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
-                    "frac": round(achieved_gbs / hbm, 4)}
-    else:
-        ach = flops_per / t_compute / 1e12
-        roofline = {"bound": "tensor", "achieved": round(ach, 2), "peak": tc, "unit": "TFLOP/s",
-                    "frac": round(ach / tc, 4)}
+    roofline = roofline_of(alg, t_compute, peaks)
     tr = recorded_traffic(args.workload)
     roofline["traffic"] = tr
     roofline["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
-    roofline["kernel"] = "csgmv_qkv (shrink->expand, h on chip or in the workspace)" \
-        if not isinstance(w0, wl.EmbeddingWorkload) else "embedding_lora_a"
-    roofline["algorithmic_bytes_per_launch"] = int(bytes_per)
-    roofline["algorithmic_flops_per_launch"] = int(flops_per)
+    roofline["kernel"] = ("embedding_lora_a" if isinstance(w0, wl.EmbeddingWorkload) else
+                          "csgmv_qkv call (" + ("shrink + expand kernels through the workspace"
+                                                if kernels == 2 else "one fused kernel") + ")")
+    roofline["algorithmic_bytes_per_launch"] = int(alg["bytes"])
+    roofline["algorithmic_flops_per_launch"] = int(alg["flops"])
     roofline["kernel_us"] = round(t_compute * 1e6, 3)
-    roofline["roofline_us"] = round(max(t_hbm, t_tc) * 1e6, 3)
+    roofline["timed_calls"] = k_compute
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -433,23 +526,60 @@ def run_gpu(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w0.name, "tokens_per_step": tokens_per_step, "chunk_size": chunk,
                    "input_sets": nsets, "set_bytes": per_set,
-                   "l2": f"rotating {nsets} input sets ({nsets * per_set / 1e6:.0f} MB > 2x L2) instead of a flush",
+                   "l2": (f"rotating {nsets} input sets ({nsets * per_set / 1e6:.0f} MB > 2x L2) instead of a flush"
+                          if nsets > 1 else f"one input set of {per_set / 1e6:.0f} MB (> 2x L2) instead of a flush"),
                    "step": "csgmv_build_batch_info + " + ("embedding_lora_a" if isinstance(w0, wl.EmbeddingWorkload)
                                                           else "csgmv_qkv"),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": roofline,
-        "breakdown_us": {"build_batch_info": round(t_build * 1e6, 3), "fused": round(t_compute * 1e6, 3),
-                         "step": round(elapsed / k_steps * 1e6, 3)},
-        "gpu_launches": (1 + qkv_kernels(w0, sets[0].bi)) * k_steps,
+        "breakdown_us": breakdown,
+        "gpu_launches": (1 + kernels) * k_steps,
         "clocks": clocks,
         "e2e": e2e,
     }
+    if rank == 0 and world == 1 and not args.no_per_config:
+        per = {}
+        with ClockSampler(local) as clk2:
+            for label, workload, ch in PER_CONFIG:
+                if workload == args.workload and ch == chunk_override:
+                    continue
+                per[label] = measure_config(torch, label, workload, ch, peaks)
+        per["clocks"] = clk2.summary()
+        line["per_config"] = per
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(ws, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def time_split_kernels(torch, sets) -> dict:
+    """CUDA-event time of the two kernels of the workspace path on their own:
+    csgmv_shrink into an fp32 h buffer, then csgmv_expand from it (the same
+    kernels csgmv_qkv launches there)."""
+    from segmented_gather_gemm_gb300 import binding as B
+    hs = []
+    for s in sets:
+        w = s.w
+        hs.append(s.ws[: w.s * w.c * w.R].view(w.s, w.c * w.R))
+
+    class _Shrink:
+        def __init__(self, s, h):
+            self.s, self.h = s, h
+
+        def compute(self):
+            s = self.s
+            B.csgmv_shrink(s.x, s.A, s.w.c, self.h, s.bi)
+
+    class _Expand(_Shrink):
+        def compute(self):
+            s = self.s
+            B.csgmv_expand(self.h, s.B, s.w.offsets, s.w.c, s.widest, s.y, True, s.bi)
+
+    t_s, _ = time_kind(torch, [_Shrink(s, h) for s, h in zip(sets, hs)], "compute")
+    t_e, _ = time_kind(torch, [_Expand(s, h) for s, h in zip(sets, hs)], "compute")
+    return {"shrink": round(t_s * 1e6, 3), "expand": round(t_e * 1e6, 3)}
 
 
 def run_e2e(torch, w, chunk_override, steps, world):
@@ -598,10 +728,10 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2400)
-    ap.add_argument("--warmup", type=int, default=48)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode_qkv",
+    ap.add_argument("--workload", default="prefill_gate_up",
                     choices=["decode_qkv", "prefill_gate_up", "skewed_down_proj", "lm_head_decode", "lm_head_pruned",
                              "tiny", "embedding"])
     ap.add_argument("--chunk", type=int, default=128, help="chunk size of skewed_down_proj")
@@ -610,6 +740,7 @@ def main():
     ap.add_argument("--sets", type=int, default=0, help="input sets to rotate (0 = enough to defeat L2)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the other configurations")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="seconds of untimed steps before the timed region, under the clock sampler")

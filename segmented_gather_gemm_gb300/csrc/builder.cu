@@ -9,6 +9,10 @@
 // contiguous in token order and stay contiguous in sorted order, so each
 // request only needs its destination offset
 //     dest[i] = (tokens of slots < a_i) + (tokens of earlier requests on a_i).
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "csgmv_internal.h"
 
 namespace csgmv {
@@ -414,19 +418,31 @@ build_lm_head_kernel(BuildParams p, csgmv_batch_info bi) {
     }
 }
 
+// Lets `fn` take up to 227 KB of dynamic shared memory on the current
+// device.  The attribute belongs to the kernel on each device, so it is set
+// once per (kernel, device), under a lock for callers on several threads.
+cudaError_t allow_large_smem(const void *fn) {
+    static std::mutex mu;
+    static std::set<std::pair<const void *, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.count({fn, dev})) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    done.insert({fn, dev});
+    return cudaSuccess;
+}
+
 }  // namespace
 
 size_t build_lm_head_smem_bytes(int bs) { return sizeof(int) * ((size_t)bs + 1 + kWarps + 2); }
 
 cudaError_t launch_build_lm_head(const BuildParams &p, const csgmv_batch_info &bi, cudaStream_t stream) {
     size_t smem = build_lm_head_smem_bytes(p.bs);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(build_lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             227 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t e = allow_large_smem(reinterpret_cast<const void *>(build_lm_head_kernel));
+    if (e != cudaSuccess) return e;
     build_lm_head_kernel<<<1, kBuildThreads, smem, stream>>>(p, bi);
     return cudaGetLastError();
 }
@@ -437,13 +453,8 @@ size_t build_smem_bytes(int bs, int max_loras) {
 
 cudaError_t launch_build(const BuildParams &p, const csgmv_batch_info &bi, cudaStream_t stream) {
     size_t smem = build_smem_bytes(p.bs, bi.max_loras);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(build_batch_info_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t e = allow_large_smem(reinterpret_cast<const void *>(build_batch_info_kernel));
+    if (e != cudaSuccess) return e;
     build_batch_info_kernel<<<1, kBuildThreads, smem, stream>>>(p, bi);
     return cudaGetLastError();
 }

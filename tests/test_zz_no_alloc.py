@@ -3,20 +3,25 @@ workspace when they call it.
 
 Such callers (an engine that plans all device memory up front and hands the
 kernel only its own tensors, or code that must not call cudaMalloc or a
-caching allocator at that point) still get the two-kernel prefill path: the
-library keeps a fixed 32 MiB device array for h.  These tests run it through
-the C ABI on two different batches in a row, so that anything a call left in
-the shared array would show up in the next one, and compare each result with
-csgmv_qkv given an ordinary workspace.  This file sorts last so that a run
+caching allocator at that point) still get the two-kernel path: the library
+keeps a fixed 32 MiB device array for h.  These tests run it through the C
+ABI on two different batches in a row, so that anything a call left in the
+shared array would show up in the next one, and compare each result with
+csgmv_qkv given an ordinary workspace and with the fp64 oracle.  Every case
+is one the library runs as two kernels through h (asserted with the
+benchmark's launch-count rule), so the shared array is really used: a
+prefill-shaped batch (128-token tiles) and a vocabulary-wide decode batch
+(16-token tiles, 32768 columns or more).  This file sorts last so that a run
 that stops at its first failure has already run every other test.
 """
 import numpy as np
 import pytest
 import torch
 
+import bench
 from segmented_gather_gemm_gb300 import binding as B
 from segmented_gather_gemm_gb300 import workloads as wl
-from tests.gpu_helpers import assert_close, build_batch, dev_bf16, host_f64
+from tests.gpu_helpers import assert_close, build_batch, dev_bf16, host_f64, oracle_fused
 
 pytestmark = pytest.mark.gpu
 
@@ -28,8 +33,16 @@ def _prefill_case(seed):
                           rank_choices=list(range(1, 33)), zero_rank_prob=0.2, std=0.5, min_len=200)
 
 
+def _wide_decode_case(seed):
+    # one token per request on 8 slots (16-token tiles) onto 33024 columns:
+    # the expand-only launch spreads column blocks over every SM
+    return wl.random_lora(seed, bs=24, max_len=1, K=512, N_slices=[33024], R=16, L=8,
+                          rank_choices=[5, 8, 16], zero_rank_prob=0.1, std=0.5, min_len=1)
+
+
 def _run(w, static):
     bi = build_batch(w)
+    assert bench.qkv_kernels(w, bi) == 2, "the case must take the two-kernel path"
     x, A, Bm, y = dev_bf16(w.x), dev_bf16(w.A), dev_bf16(w.B), dev_bf16(w.base)
     widest = int(np.max(np.diff(w.offsets)))
     if static:
@@ -43,12 +56,14 @@ def _run(w, static):
     return host_f64(y)
 
 
-def test_static_scratch_matches_csgmv_qkv_on_two_calls_in_a_row():
+@pytest.mark.parametrize("make", [_prefill_case, _wide_decode_case], ids=["prefill", "wide-decode"])
+def test_static_scratch_matches_csgmv_qkv_on_two_calls_in_a_row(make):
     for seed in (11, 12):  # the second call finds the first call's h in the array
-        w = _prefill_case(seed)
+        w = make(seed)
         got = _run(w, static=True)
         ref = _run(w, static=False)
         assert_close(got, ref, f"static scratch vs csgmv_qkv, seed {seed}")
+        assert_close(got, oracle_fused(w), f"static scratch vs oracle, seed {seed}")
 
 
 def test_static_scratch_rejects_a_batch_too_large_for_it():
