@@ -99,6 +99,15 @@ int check_rank(const csgmv_batch_info *bi) {
     return CSGMV_OK;
 }
 
+// B as one (max_loras, N, R) tensor: every slice reads rows w * N + n of it.
+void single_b(csgmv::LoraParams &p) {
+    for (int j = 0; j < csgmv::kMaxSlices; ++j) {
+        p.Bs[j] = p.B;
+        p.b_rows[j] = (int)p.N;
+        p.b_row0[j] = j < p.c ? p.off[j] : 0;
+    }
+}
+
 void fill_common(csgmv::LoraParams &p, const csgmv_batch_info *bi) {
     p.seg_indptr = bi->seg_indptr;
     p.weight_indices = bi->weight_indices;
@@ -278,6 +287,7 @@ int csgmv_expand(const void *h, int h_dtype, int64_t ldh, const void *B, int64_t
     p.N = N;
     p.c = num_slices;
     for (int j = 0; j <= num_slices; ++j) p.off[j] = slice_offsets[j];
+    single_b(p);
     p.accumulate = accumulate ? 1 : 0;
     cudaError_t e = csgmv::launch_lora(csgmv::kModeExpand, p, *bi, reinterpret_cast<cudaStream_t>(stream), nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "csgmv_expand launch");
@@ -315,6 +325,7 @@ int csgmv_qkv(const void *x, int64_t K, const void *A, const void *B, int64_t N,
     p.N = N;
     p.c = num_slices;
     for (int j = 0; j <= num_slices; ++j) p.off[j] = slice_offsets[j];
+    single_b(p);
     p.accumulate = 1;
     const size_t hbytes = (size_t)s * num_slices * bi->max_rank * 4;
     if (workspace && workspace_bytes >= hbytes && csgmv::qkv_split_pays(p, *bi)) {

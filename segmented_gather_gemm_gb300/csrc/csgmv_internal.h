@@ -35,6 +35,11 @@ struct LoraParams {
     const uint16_t *x;   // (s, K) bf16
     const uint16_t *A;   // (max_loras, c*R, K) bf16
     const uint16_t *B;   // (max_loras, N, R) bf16
+    // B of slice j as its own tensor: rows w * b_rows[j] + b_row0[j] + (n - off[j])
+    // of Bs[j] (R bf16 each) hold B[w][n] for n in slice j.  One (L, N, R)
+    // tensor is Bs[j] = B, b_rows[j] = N, b_row0[j] = off[j].
+    const uint16_t *Bs[kMaxSlices];
+    int b_rows[kMaxSlices], b_row0[kMaxSlices];
     uint16_t *y;         // (s, N) bf16, in/out
     void *h;             // (s, ldh) bf16 or f32 (shrink output / expand input)
     int64_t K, N, ldh;

@@ -8,6 +8,7 @@
 #include <tuple>
 
 #include "lora_small.cuh"
+#include "lora_stream.cuh"
 #include "lora_ws.cuh"
 
 namespace csgmv {
@@ -17,6 +18,7 @@ const void *lora_kernel_shrink(int tm, int rmax, bool tc);
 const void *lora_kernel_expand(int tm, int rmax, bool tc);
 const void *lora_kernel_ws(int mode, int rmax);
 const void *lora_kernel_small(int mode, int tm, int rmax);
+const void *lora_kernel_stream();
 
 namespace {
 
@@ -483,6 +485,103 @@ cudaError_t launch_lora_ws(int mode, LoraParams &p, const csgmv_batch_info &bi, 
     return cudaGetLastError();
 }
 
+// Shared-memory carve-up of the streaming expand kernel for ring depth S;
+// returns the bytes needed (with slack for aligning the window to 1024).
+size_t carve_stream(StreamParams &k, int S) {
+    size_t off = 0;
+    auto take = [&](size_t bytes, size_t align) {
+        off = align_up(off, align);
+        size_t o = off;
+        off += bytes;
+        return (int)o;
+    };
+    k.S = S;
+    k.slot_bytes = kStTileBytes + kStCols * k.p.R * 2;
+    k.o_bar = take((size_t)(4 * S + 2 * kStAcc + 4) * 8 + 16, 16);
+    k.o_run = take((size_t)(5 * k.runcap + 1 + 32) * 4, 16);
+    k.o_tok = take((size_t)(2 * 128 + 4) * 4, 16);
+    k.o_op = take((size_t)4 * kStTileBytes, 1024);
+    k.o_ring = take((size_t)S * k.slot_bytes, 1024);
+    // at least 116 KB, so that one CTA holds an SM (and its 512 TMEM columns)
+    return std::max(off + 1024, (size_t)116 * 1024);
+}
+
+// Expand-only calls on 128-token tiles: the streaming tcgen05 kernel, one CTA
+// per SM.  Units are (tile, column block inside one slice); the column block
+// is sized so that every CTA gets about sixteen units.
+cudaError_t launch_lora_stream(LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream, LaunchInfo *info) {
+    const void *fn = lora_kernel_stream();
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    StreamParams k;
+    memset(&k, 0, sizeof k);
+    k.p = p;
+    k.max_segments = bi.max_segments;
+    k.runcap = std::max(1, std::min(bi.max_segments, bi.max_loras + std::max(bi.max_bs, 1)));
+    const size_t budget = 227 * 1024;
+    int S = 8;
+    size_t smem = carve_stream(k, S);
+    while (smem > budget && S > 3) smem = carve_stream(k, --S);
+    if (smem > budget) return cudaErrorInvalidConfiguration;
+    e = ensure_attrs(fn, dev, 1);
+    if (e != cudaSuccess) return e;
+    int res = 0;
+    e = resident(fn, dev, 1, smem, &res, kStThreads);
+    if (e != cudaSuccess) return e;
+    if (res < 1) return cudaErrorInvalidConfiguration;
+
+    const int s = p.num_tokens;
+    const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
+    const int tiles_est = (s + 127) / 128 + slots / 2;
+    const int tiles_ub = (s + 127) / 128 + std::min(std::max(bi.bs, 1), std::max(bi.max_loras, 1));
+    const int64_t ncols = p.off[p.c] - p.off[0];
+    int64_t cb = (int64_t)tiles_est * ncols / ((int64_t)16 * res);
+    cb = std::max<int64_t>(512, (cb + 63) / 64 * 64);
+    k.cb = (int)std::min<int64_t>(cb, 1 << 30);
+    k.upt = 0;
+    for (int j = 0; j < p.c; ++j) k.upt += (p.off[j + 1] - p.off[j] + k.cb - 1) / k.cb;
+    if (k.upt == 0) return cudaSuccess;  // no columns
+    const int64_t units_ub = (int64_t)tiles_ub * k.upt;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(res, units_ub));
+
+    const int L = bi.max_loras;
+    bool ok = true;
+    for (int j = 0; j < kMaxSlices; ++j) {
+        const int jj = j < p.c ? j : 0;
+        ok = ok && encode_2d(&k.tmB[j], p.Bs[jj], (uint64_t)p.R, (uint64_t)L * p.b_rows[jj], (uint64_t)p.R * 2, p.R,
+                             kStCols, swizzle_for_row_bytes(p.R * 2));
+    }
+    ok = ok && encode_2d(&k.tmY, p.y, (uint64_t)p.N, (uint64_t)s, (uint64_t)p.N * 2, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && encode_2d(&k.tmYs, p.y, (uint64_t)p.N, (uint64_t)s, (uint64_t)p.N * 2, 64, 32,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && encode_2d(&k.tmYg, p.y, (uint64_t)p.N, (uint64_t)s, (uint64_t)p.N * 2, 64, 1,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) return cudaErrorInvalidValue;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kStThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    set_dependent_launch(&attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (info) {
+        info->tm = 128;
+        info->crmax = p.R;
+        info->cluster = 1;
+        info->grid = grid;
+        info->smem = smem;
+    }
+    void *args[1] = {&k};
+    e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 // Token tile for a batch: 16 for one or two tokens per slot run, 32 for a few,
 // 128 for prefill.
 int token_tile(const LoraParams &p, const csgmv_batch_info &bi) {
@@ -523,6 +622,9 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
     // and expand calls measure faster on the cluster kernel.
     if (tm == 128 && p.R >= 16 && mode == kModeShrink && p.K <= 4096)
         return launch_lora_ws(mode, p, bi, stream, info, rmax);
+    // Expand-only calls on 128-token tiles stream base through the
+    // warp-specialized tcgen05 expand.
+    if (tm == 128 && p.R >= 16 && mode == kModeExpand) return launch_lora_stream(p, bi, stream, info);
     if (tm <= 32) {
         const cudaError_t es = launch_lora_small(mode, p, bi, stream, info, rmax, tm);
         if (es != cudaErrorInvalidConfiguration) return es;

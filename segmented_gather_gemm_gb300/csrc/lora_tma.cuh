@@ -136,20 +136,21 @@ __device__ __forceinline__ int block_scan(int v, int *scratch, int *total) {
 
 // Slot runs of the batch info and their token tiles (see the file comment).
 // Returns the number of tiles; the tables live in shared memory.
+// `tables` holds 5 * runcap + 1 + 32 ints; every thread of the block calls it.
 template <int TM>
-__device__ int build_run_table(const TmaKernelParams &k, unsigned char *smem, int *nruns_out) {
-    const LoraParams &p = k.p;
-    int *run_seg = reinterpret_cast<int *>(smem + k.o_run);
-    int *run_p0 = run_seg + k.runcap;
-    int *run_len = run_p0 + k.runcap;
-    int *run_w = run_len + k.runcap;
-    int *run_tp = run_w + k.runcap;        // [runcap + 1]
-    int *scratch = run_tp + k.runcap + 1;  // [32]
+__device__ int build_run_table_raw(const LoraParams &p, int max_segments, int runcap, int *tables,
+                                   int *nruns_out) {
+    int *run_seg = tables;
+    int *run_p0 = run_seg + runcap;
+    int *run_len = run_p0 + runcap;
+    int *run_w = run_len + runcap;
+    int *run_tp = run_w + runcap;        // [runcap + 1]
+    int *scratch = run_tp + runcap + 1;  // [32]
     const int tid = threadIdx.x, nt = blockDim.x;
     griddep_wait();  // the batch info may come from the kernel launched just before
     // Every word a thread needs is loaded in one round, bounded by the
     // capacity rather than by the segment count (which is loaded alongside).
-    const int cap = k.max_segments;
+    const int cap = max_segments;
     const int nseg_raw = *p.num_segments_dev;
     int carry = 0;
     for (int k0 = 0; k0 < cap; k0 += nt) {
@@ -168,15 +169,15 @@ __device__ int build_run_table(const TmaKernelParams &k, unsigned char *smem, in
         int tot;
         const int pre = block_scan(st, scratch, &tot);
         const int run = carry + pre + st - 1;  // run of segment s
-        if (st && run < k.runcap) {
+        if (st && run < runcap) {
             run_w[run] = w_here;
             run_p0[run] = max(0, min(ip0, p.num_tokens));
         }
-        if (en && run >= 0 && run < k.runcap) run_len[run] = max(0, min(ip1, p.num_tokens));  // run end for now
+        if (en && run >= 0 && run < runcap) run_len[run] = max(0, min(ip1, p.num_tokens));  // run end for now
         carry += tot;
     }
     int nruns = carry;
-    if (nruns > k.runcap) {
+    if (nruns > runcap) {
         if (tid == 0) atomicOr(p.status, CSGMV_STATUS_CAPACITY);
         nruns = 0;
     }
@@ -199,6 +200,35 @@ __device__ int build_run_table(const TmaKernelParams &k, unsigned char *smem, in
     __syncthreads();
     *nruns_out = nruns;
     return tcarry;
+}
+
+template <int TM>
+__device__ int build_run_table(const TmaKernelParams &k, unsigned char *smem, int *nruns_out) {
+    return build_run_table_raw<TM>(k.p, k.max_segments, k.runcap, reinterpret_cast<int *>(smem + k.o_run),
+                                   nruns_out);
+}
+
+// Slot, first sorted position and size of token tile `tile` (run table of
+// build_run_table_raw).
+template <int TM>
+__device__ __forceinline__ Unit tile_of(const int *tables, int runcap, int nruns, int tile) {
+    const int *run_seg = tables;
+    const int *run_p0 = run_seg + runcap;
+    const int *run_len = run_p0 + runcap;
+    const int *run_w = run_len + runcap;
+    const int *run_tp = run_w + runcap;
+    Unit U;
+    U.nb = 0;
+    int lo = 0, hi = nruns;  // last run with run_tp <= tile
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (run_tp[mid] <= tile) lo = mid; else hi = mid;
+    }
+    const int t_in = tile - run_tp[lo];
+    U.w = run_w[lo];
+    U.p0 = run_p0[lo] + t_in * TM;
+    U.M = min(TM, run_len[lo] - t_in * TM);
+    return U;
 }
 
 template <int TM>

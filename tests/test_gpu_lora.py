@@ -57,6 +57,10 @@ def test_fused_with_workspace_matches_oracle(case):
         y, bi = run_fused(w, base=base, workspace=True)
         assert bi.device_status() == 0
         assert_close(f64(y), oracle_fused(w, base=base), f"fused+workspace base={base} {case}")
+    # NaN in every padding row of A and column of B changes nothing
+    y0, _ = run_fused(w, workspace=True)
+    y1, _ = run_fused(make(*case, pad=float("nan")), workspace=True)
+    assert np.array_equal(y0, y1), f"padding leaked into the output ({case})"
 
 
 # (seed, bs, max_len, K, slices, R, L): short requests on a handful of slots and
