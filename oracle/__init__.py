@@ -18,6 +18,10 @@ What each function follows (sglang, as printed on the pages):
                        run_lora_b_sgemm / run_qkv_lora (slice_offsets, base_output)
   fused                chunked_backend.py, run_qkv_lora / run_gate_up_lora
   embedding            base_backend.py, run_lora_a_embedding
+  fused_sliced,        base_backend.py, run_qkv_lora / run_gate_up_lora (B as a
+  expand_sliced        tuple of per-slice buffers)
+  embedding_extra      base_backend.py, run_lora_a_embedding (extra_embeddings)
+  extra_token_embedding  base_backend.py, run_extra_token_embedding
 """
 from __future__ import annotations
 
@@ -94,6 +98,21 @@ def _bind(lib):
     lib.oracle_embedding.restype = ctypes.c_int
     lib.oracle_embedding.argtypes = [_i32p, ctypes.c_int64, _u16p, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int64, _i32p, _i32p, _u16p]
+    _u16pp = ctypes.POINTER(_u16p)
+    lib.oracle_expand_sliced.restype = ctypes.c_int
+    lib.oracle_expand_sliced.argtypes = [_f64p, ctypes.c_int64, ctypes.c_int64, _u16pp, ctypes.c_int64,
+                                         ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, _i32p, _i32p,
+                                         _f32p, _u16p, _f64p]
+    lib.oracle_fused_sliced.restype = ctypes.c_int
+    lib.oracle_fused_sliced.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int64, _u16p, _u16pp,
+                                        ctypes.c_int64, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int,
+                                        _i32p, _i32p, _f32p, _u16p, _f64p]
+    lib.oracle_embedding_extra.restype = ctypes.c_int
+    lib.oracle_embedding_extra.argtypes = [_i32p, ctypes.c_int64, _u16p, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int64, _u16p, ctypes.c_int64, _i32p, _i32p, _u16p]
+    lib.oracle_extra_token_embedding.restype = ctypes.c_int
+    lib.oracle_extra_token_embedding.argtypes = [_i32p, ctypes.c_int64, _u16p, ctypes.c_int64, _u16p,
+                                                 ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _i32p]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_set_num_threads.restype = None
@@ -265,4 +284,87 @@ def embedding(ids, A_emb_bits, token_adapter_arr, ranks) -> tuple[np.ndarray, in
     out = np.zeros((s, R), np.uint16)
     bad = _load().oracle_embedding(_p(idv, _i32p), s, _p(A, _u16p), L, R, V, _p(ta, _i32p),
                                    _p(rk, _i32p), _p(out, _u16p))
+    return out, int(bad)
+
+
+def _slice_ptrs(B_slices, c):
+    """Per-slice (L, width_j, R) bf16 bit arrays -> (kept arrays, C pointer array, R)."""
+    keep = [_c(b, np.uint16) for b in B_slices]
+    assert len(keep) == c
+    R = keep[0].shape[2]
+    arr = (_u16p * c)(*[b.ctypes.data_as(_u16p) for b in keep])
+    return keep, arr, R
+
+
+def expand_sliced(h, B_slices, offsets, c: int, token_adapter_arr, ranks, scalings, base_bits=None) -> np.ndarray:
+    """y (s, N) fp64 with B given per slice: B_slices[j] is (L, off[j+1]-off[j], R) bf16 bits."""
+    hh = _c(h, np.float64)
+    off = _c(offsets, np.int32)
+    keep, arr, R = _slice_ptrs(B_slices, c)
+    L = keep[0].shape[0]
+    N = int(off[-1])
+    s = hh.shape[0]
+    ta = _c(token_adapter_arr, np.int32)
+    rk = _c(ranks, np.int32)
+    sc = _c(scalings, np.float32)
+    base = None if base_bits is None else _c(base_bits, np.uint16)
+    if base is not None:
+        N = base.shape[1]
+    y = np.zeros((s, N), np.float64)
+    _load().oracle_expand_sliced(_p(hh, _f64p), hh.shape[1], s, arr, N, L, R, _p(off, _i32p), c,
+                                 _p(ta, _i32p), _p(rk, _i32p), _p(sc, _f32p), _p(base, _u16p), _p(y, _f64p))
+    return y
+
+
+def fused_sliced(x_bits, A_bits, B_slices, offsets, c: int, token_adapter_arr, ranks, scalings,
+                 base_bits=None) -> np.ndarray:
+    """y (s, N) fp64 = base + sigma_w * B_j,w (A_w x) per slice j, with B given
+    per slice (B_slices[j] of shape (L, off[j+1]-off[j], R)), h kept in fp64."""
+    x = _c(x_bits, np.uint16)
+    A = _c(A_bits, np.uint16)
+    s, K = x.shape
+    L, cR, _ = A.shape
+    off = _c(offsets, np.int32)
+    keep, arr, R = _slice_ptrs(B_slices, c)
+    assert cR == c * R
+    ta = _c(token_adapter_arr, np.int32)
+    rk = _c(ranks, np.int32)
+    sc = _c(scalings, np.float32)
+    base = None if base_bits is None else _c(base_bits, np.uint16)
+    N = base.shape[1] if base is not None else int(off[-1])
+    y = np.zeros((s, N), np.float64)
+    _load().oracle_fused_sliced(_p(x, _u16p), s, K, _p(A, _u16p), arr, N, L, R, _p(off, _i32p), c,
+                                _p(ta, _i32p), _p(rk, _i32p), _p(sc, _f32p), _p(base, _u16p), _p(y, _f64p))
+    return y
+
+
+def embedding_extra(ids, A_emb_bits, extra_bits, token_adapter_arr, ranks) -> tuple[np.ndarray, int]:
+    """(out (s, R) bf16 bits, bad rows) with extra tokens: ids in [V, V + E)
+    read extra (L, E, R)."""
+    idv = _c(ids, np.int32)
+    A = _c(A_emb_bits, np.uint16)
+    L, R, V = A.shape
+    ex = _c(extra_bits, np.uint16)
+    assert ex.shape[0] == L and ex.shape[2] == R
+    E = ex.shape[1]
+    s = len(idv)
+    ta = _c(token_adapter_arr, np.int32)
+    rk = _c(ranks, np.int32)
+    out = np.zeros((s, R), np.uint16)
+    bad = _load().oracle_embedding_extra(_p(idv, _i32p), s, _p(A, _u16p), L, R, V, _p(ex, _u16p), E,
+                                         _p(ta, _i32p), _p(rk, _i32p), _p(out, _u16p))
+    return out, int(bad)
+
+
+def extra_token_embedding(ids, output_bits, extra_bits, vocab_size: int, token_adapter_arr) -> tuple[np.ndarray, int]:
+    """(output (s, D) bf16 bits with the rows of extra tokens replaced, bad rows)."""
+    idv = _c(ids, np.int32)
+    out = np.array(output_bits, dtype=np.uint16, copy=True, order="C")
+    ex = _c(extra_bits, np.uint16)
+    L, E, D = ex.shape
+    s = len(idv)
+    assert out.shape == (s, D)
+    ta = _c(token_adapter_arr, np.int32)
+    bad = _load().oracle_extra_token_embedding(_p(idv, _i32p), s, _p(out, _u16p), D, _p(ex, _u16p), L, E,
+                                               int(vocab_size), _p(ta, _i32p))
     return out, int(bad)

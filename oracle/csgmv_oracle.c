@@ -347,6 +347,57 @@ int oracle_fused(const uint16_t *x, int64_t s, int64_t K, const uint16_t *A, con
 }
 
 /* ------------------------------------------------------------------------- *
+ * Expand with tuple-form B.  [BB] run_qkv_lora: qkv_lora_b may be a tuple of
+ * a q buffer (1, L, N_q, R) and a combined kv buffer (2, L, N_kv, R); [BB]
+ * run_gate_up_lora: a tuple of two (L, N_out, R) buffers.  Either way slice j
+ * of the output has a B of its own, Bs[j] of shape (L, off[j+1] - off[j], R),
+ * whose row 0 is output column off[j]:
+ *     y[t][n] = base[t][n] + sigma * sum_{k<r} h[t][j*r + k] * Bs[j][w][n - off[j]][k]
+ * for n in [off[j], off[j+1]).  Everything else as oracle_expand.
+ * ------------------------------------------------------------------------- */
+int oracle_expand_sliced(const double *h, int64_t ldh, int64_t s, const uint16_t *const *Bs, int64_t N, int L,
+                         int R, const int32_t *off, int c, const int32_t *token_adapter, const int32_t *ranks,
+                         const float *scalings, const uint16_t *base, double *y)
+{
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 8) reduction(+ : bad)
+    for (int64_t t = 0; t < s; ++t) {
+        double *yt = y + t * N;
+        for (int64_t n = 0; n < N; ++n)
+            yt[n] = base ? oracle_bf16_to_f64(base[t * N + n]) : 0.0;
+        int w = token_adapter[t];
+        if (w < 0 || w >= L) { bad += 1; continue; }
+        int r = ranks[w];
+        double sigma = (double)scalings[w];
+        const double *ht = h + t * ldh;
+        for (int j = 0; j < c; ++j) {
+            const int64_t width = (int64_t)off[j + 1] - off[j];
+            const uint16_t *Bw = Bs[j] + (int64_t)w * width * R;
+            for (int64_t n = off[j]; n < off[j + 1]; ++n) {
+                double acc = 0.0;
+                for (int k = 0; k < r; ++k)
+                    acc += oracle_bf16_to_f64(Bw[(n - off[j]) * R + k]) * ht[(int64_t)j * r + k];
+                yt[n] += acc * sigma;
+            }
+        }
+    }
+    return bad;
+}
+
+/* Fused shrink then expand with tuple-form B, h in fp64. */
+int oracle_fused_sliced(const uint16_t *x, int64_t s, int64_t K, const uint16_t *A, const uint16_t *const *Bs,
+                        int64_t N, int L, int R, const int32_t *off, int c, const int32_t *token_adapter,
+                        const int32_t *ranks, const float *scalings, const uint16_t *base, double *y)
+{
+    const int64_t cR = (int64_t)c * R;
+    double *h = (double *)malloc(sizeof(double) * (size_t)(s > 0 ? s * cR : 1));
+    int bad = oracle_shrink(x, s, K, A, L, c, R, token_adapter, ranks, h);
+    oracle_expand_sliced(h, cR, s, Bs, N, L, R, off, c, token_adapter, ranks, scalings, base, y);
+    free(h);
+    return bad;
+}
+
+/* ------------------------------------------------------------------------- *
  * Embedding LoRA-A gather.  [BB] run_lora_a_embedding: input_ids (s,),
  * weights (L, R, V) -> (s, R); [CB] run_lora_a_embedding (no extra tokens).
  *     out[t][k] = A_emb[w][k][ids[t]]  for k < r_w,  0 for r_w <= k < R.
@@ -366,6 +417,59 @@ int oracle_embedding(const int32_t *ids, int64_t s, const uint16_t *A_emb, int L
         int r = ranks[w];
         for (int k = 0; k < r && k < R; ++k)
             ot[k] = A_emb[((int64_t)w * R + k) * V + id];
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------- *
+ * Embedding LoRA-A gather with extra tokens.  [BB] run_lora_a_embedding:
+ * tokens with ids >= vocab_size are extra tokens, whose LoRA-A rows come from
+ * extra_embeddings (L, num_extra, R):
+ *     out[t][k] = A_emb[w][k][id]          for 0 <= id < V,
+ *     out[t][k] = extra[w][id - V][k]      for V <= id < V + num_extra,
+ * for k < r_w, and 0 for r_w <= k < R (the rank rule of oracle_embedding).
+ * Any other id, or a slot outside [0, L), leaves the row 0 and is counted.
+ * ------------------------------------------------------------------------- */
+int oracle_embedding_extra(const int32_t *ids, int64_t s, const uint16_t *A_emb, int L, int R, int64_t V,
+                           const uint16_t *extra, int64_t num_extra, const int32_t *token_adapter,
+                           const int32_t *ranks, uint16_t *out)
+{
+    int bad = 0;
+    for (int64_t t = 0; t < s; ++t) {
+        uint16_t *ot = out + t * R;
+        for (int k = 0; k < R; ++k) ot[k] = 0;
+        int w = token_adapter[t];
+        int64_t id = ids[t];
+        if (w < 0 || w >= L || id < 0 || id >= V + num_extra) { ++bad; continue; }
+        const int rr = ranks[w] < R ? ranks[w] : R;
+        for (int k = 0; k < rr; ++k) {
+            if (id < V) ot[k] = A_emb[((int64_t)w * R + k) * V + id];
+            else ot[k] = extra[((int64_t)w * num_extra + (id - V)) * R + k];
+        }
+    }
+    return bad;
+}
+
+/* ------------------------------------------------------------------------- *
+ * Extra-token embedding.  [BB] run_extra_token_embedding: output (s, D) is
+ * modified in place with extra_embeddings (L, num_extra, D): the row of every
+ * token with V <= id < V + num_extra becomes extra[w][id - V][:] (the base
+ * vocabulary has no embedding for it); rows of ids below V are untouched.  An
+ * id outside [0, V + num_extra), or a slot outside [0, L), leaves the row
+ * untouched and is counted.
+ * ------------------------------------------------------------------------- */
+int oracle_extra_token_embedding(const int32_t *ids, int64_t s, uint16_t *output, int64_t D,
+                                 const uint16_t *extra, int L, int64_t num_extra, int64_t V,
+                                 const int32_t *token_adapter)
+{
+    int bad = 0;
+    for (int64_t t = 0; t < s; ++t) {
+        int w = token_adapter[t];
+        int64_t id = ids[t];
+        if (w < 0 || w >= L || id < 0 || id >= V + num_extra) { ++bad; continue; }
+        if (id < V) continue;
+        for (int64_t d = 0; d < D; ++d)
+            output[t * D + d] = extra[((int64_t)w * num_extra + (id - V)) * D + d];
     }
     return bad;
 }

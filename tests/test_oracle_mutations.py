@@ -35,8 +35,16 @@ MUTATIONS = [
      ["lm_head"]),
     ("lm_head_no_merge", "if (nruns > 0 && run_slot[nruns - 1] == req_adapter[i]) {",
      "if (nruns < 0) {", ["lm_head"]),
-    ("expand_uses_max_rank", "for (int k = 0; k < r; ++k)\n                    acc += ht",
-     "for (int k = 0; k < R; ++k)\n                    acc += ht", ["fused_dense", "padding"]),
+    ("expand_uses_max_rank", "for (int k = 0; k < r; ++k)\n                    acc += ht[(int64_t)j * r + k] * oracle_bf16_to_f64(Bw[n * R + k]);",
+     "for (int k = 0; k < R; ++k)\n                    acc += ht[(int64_t)j * r + k] * oracle_bf16_to_f64(Bw[n * R + k]);",
+     ["fused_dense", "padding"]),
+    ("sliced_b_global_column", "Bw[(n - off[j]) * R + k]", "Bw[n * R + k]", ["sliced_dense"]),
+    ("sliced_b_slot_stride", "Bs[j] + (int64_t)w * width * R", "Bs[j] + (int64_t)w * N * R", ["sliced_dense"]),
+    ("extra_row_off_by_one", "extra[((int64_t)w * num_extra + (id - V)) * R + k]",
+     "extra[((int64_t)w * num_extra + (id - V + 1) % num_extra) * R + k]", ["embedding_extra"]),
+    ("extra_ignores_rank", "for (int k = 0; k < rr; ++k) {", "for (int k = 0; k < R; ++k) {",
+     ["embedding_extra"]),
+    ("extra_token_overwrites_base_rows", "if (id < V) continue;", "if (id < 0) continue;", ["extra_token"]),
 ]
 
 PINS = {
@@ -50,6 +58,9 @@ PINS = {
     "rank0": pins.test_rank_zero_and_no_adapter_leave_base_exact,
     "padding": pins.test_padding_is_never_read,
     "lm_head": pins.test_lm_head_batch_info_hand_derived,
+    "sliced_dense": lambda: [pins.test_sliced_b_matches_dense_delta(s) for s in range(4)],
+    "embedding_extra": pins.test_embedding_extra_is_indexing_of_both_tables,
+    "extra_token": pins.test_extra_token_embedding_replaces_only_extra_rows,
 }
 
 

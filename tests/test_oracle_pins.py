@@ -350,3 +350,120 @@ def test_embedding_bad_ids_counted():
     ta = oracle.token_adapter(e.req_lens, e.req_adapter)
     out, bad = oracle.embedding(e.ids, e.A_emb, ta, e.ranks)
     assert bad == 2 and not out[1].any() and not out[4].any()
+
+
+# --------------------------------------------------------------------------
+# tuple-form B (base_backend.py run_qkv_lora / run_gate_up_lora docstrings)
+# --------------------------------------------------------------------------
+
+def qkv_tuple_of(B, offsets):
+    """The qkv tuple form of a single (L, N, R) B with slices q, k, v: a q
+    buffer (1, L, N_q, R) and one kv buffer (2, L, N_kv, R), as the
+    run_qkv_lora docstring lays them out (k and v of equal width)."""
+    q = B[None, :, offsets[0]:offsets[1], :].copy()
+    kv = np.stack([B[:, offsets[1]:offsets[2], :], B[:, offsets[2]:offsets[3], :]]).copy()
+    return q, kv
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_sliced_b_matches_dense_delta(seed):
+    """Per-slice B against the numpy dense per-token weight delta built from
+    each slice's own buffer (q / kv tuple for c = 3, two buffers for c = 2)."""
+    c = 3 if seed % 2 == 0 else 2
+    widths = [16, 8, 8] if c == 3 else [24, 24]
+    w = wl.random_lora(40 + seed, bs=5, max_len=6, K=40, N_slices=widths, R=7, L=4, rank_choices=[1, 3, 5, 7])
+    off = w.offsets
+    if c == 3:
+        q, kv = qkv_tuple_of(w.B, off)
+        slices = [q[0], kv[0], kv[1]]
+    else:
+        slices = [w.B[:, off[0]:off[1], :].copy(), w.B[:, off[1]:off[2], :].copy()]
+    ta = oracle.token_adapter(w.req_lens, w.req_adapter)
+    A, x = f64(w.A), f64(w.x)
+    ref = f64(w.base).copy()
+    for t in range(w.s):
+        a = ta[t]
+        r = int(w.ranks[a])
+        for j in range(c):
+            Bj = f64(slices[j])
+            dW = float(w.scalings[a]) * (Bj[a, :, :r] @ A[a, j * r:(j + 1) * r, :])
+            ref[t, off[j]:off[j + 1]] += dW @ x[t]
+    y = oracle.fused_sliced(w.x, w.A, slices, off, c, ta, w.ranks, w.scalings, w.base)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_sliced_b_equals_single_tensor():
+    """Cutting one (L, N, R) B into its slices gives the single-tensor result
+    exactly (same sums in the same order), and so does the expand alone."""
+    w = wl.random_lora(9, bs=6, max_len=7, K=48, N_slices=[32, 16, 16], R=8, L=3, rank_choices=[2, 5, 8])
+    off = w.offsets
+    slices = [w.B[:, off[j]:off[j + 1], :].copy() for j in range(w.c)]
+    ta = oracle.token_adapter(w.req_lens, w.req_adapter)
+    y1 = oracle.fused(w.x, w.A, w.B, off, w.c, ta, w.ranks, w.scalings, w.base)
+    y2 = oracle.fused_sliced(w.x, w.A, slices, off, w.c, ta, w.ranks, w.scalings, w.base)
+    assert np.array_equal(y1, y2)
+    h = oracle.shrink(w.x, w.A, w.c, ta, w.ranks)
+    e1 = oracle.expand(h, w.B, off, w.c, ta, w.ranks, w.scalings, None)
+    e2 = oracle.expand_sliced(h, slices, off, w.c, ta, w.ranks, w.scalings, None)
+    assert np.array_equal(e1, e2)
+
+
+# --------------------------------------------------------------------------
+# extra-token embeddings (base_backend.py run_lora_a_embedding,
+# run_extra_token_embedding)
+# --------------------------------------------------------------------------
+
+def _extra_case(seed, V=37, R=6, L=3, E=5, s=40):
+    rng = np.random.default_rng(seed)
+    ranks = np.array([6, 3, 0], np.int32)[:L]
+    A = wl.normal_bf16(rng, (L, R, V), 1.0)
+    extra = wl.normal_bf16(rng, (L, E, R), 1.0)
+    ids = rng.integers(0, V + E, size=s).astype(np.int32)
+    ta = rng.integers(0, L, size=s).astype(np.int32)
+    return ids, A, extra, ta, ranks, V, E
+
+
+def test_embedding_extra_is_indexing_of_both_tables():
+    """ids below V read A_emb's column, ids in [V, V + E) read the extra row,
+    both cut at the slot's rank: numpy indexing of the two tables."""
+    ids, A, extra, ta, ranks, V, E = _extra_case(3)
+    out, bad = oracle.embedding_extra(ids, A, extra, ta, ranks)
+    assert bad == 0
+    R = A.shape[1]
+    for t in range(len(ids)):
+        w, r, i = int(ta[t]), int(ranks[ta[t]]), int(ids[t])
+        want = np.zeros(R, np.uint16)
+        want[:r] = A[w, :r, i] if i < V else extra[w, i - V, :r]
+        assert np.array_equal(out[t], want), t
+    # without extra ids it is the plain gather
+    base_ids = np.where(ids < V, ids, 0).astype(np.int32)
+    o1, _ = oracle.embedding_extra(base_ids, A, extra, ta, ranks)
+    o2, _ = oracle.embedding(base_ids, A, ta, ranks)
+    assert np.array_equal(o1, o2)
+
+
+def test_embedding_extra_bad_ids_counted():
+    ids, A, extra, ta, ranks, V, E = _extra_case(4)
+    ids[[2, 5]] = [V + E, -1]
+    out, bad = oracle.embedding_extra(ids, A, extra, ta, ranks)
+    assert bad == 2 and not out[2].any() and not out[5].any()
+
+
+def test_extra_token_embedding_replaces_only_extra_rows():
+    """Rows of extra tokens become extra[w][id - V] (every column); rows of
+    base-vocabulary ids keep their bits."""
+    rng = np.random.default_rng(5)
+    V, E, D, L, s = 50, 4, 12, 3, 30
+    extra = wl.normal_bf16(rng, (L, E, D), 1.0)
+    ids = rng.integers(0, V + E, size=s).astype(np.int32)
+    ids[:3] = [V, V + E - 1, 7]
+    ta = rng.integers(0, L, size=s).astype(np.int32)
+    output = wl.normal_bf16(rng, (s, D), 1.0)
+    got, bad = oracle.extra_token_embedding(ids, output, extra, V, ta)
+    assert bad == 0
+    for t in range(s):
+        want = extra[ta[t], ids[t] - V] if ids[t] >= V else output[t]
+        assert np.array_equal(got[t], want), t
+    ids[4] = V + E
+    got2, bad2 = oracle.extra_token_embedding(ids, output, extra, V, ta)
+    assert bad2 == 1 and np.array_equal(got2[4], output[4])
