@@ -116,9 +116,8 @@ def qkv_kernels(w, bi) -> int:
     """Kernels one csgmv_qkv call launches when given a workspace: two (shrink,
     expand) where the library takes its two-kernel path, else one.  The path
     is taken by 16- / 32-token tiles with at least WIDE_COLS output columns,
-    and by 128-token tiles with K <= 4096, R >= 16 and slice offsets on
-    16-column boundaries.  Mirrors the library's choice for the gpu_launches
-    count."""
+    and by 128-token tiles with a buffer rank R >= 16.  Mirrors the library's
+    choice for the gpu_launches count."""
     if isinstance(w, wl.EmbeddingWorkload):
         return 1
     slots = max(1, min(max(w.bs, 1), w.L))
@@ -126,7 +125,7 @@ def qkv_kernels(w, bi) -> int:
     if tm <= 32:
         split = int(w.offsets[-1]) - int(w.offsets[0]) >= WIDE_COLS
     else:
-        split = w.K <= 4096 and w.R >= 16 and all(int(o) % 16 == 0 for o in w.offsets)
+        split = w.R >= 16
     return 2 if split else 1
 
 
@@ -152,7 +151,8 @@ _SHARED_SOURCES = ("lora_tma.cuh", "lora_launch.cu", "device_utils.cuh", "csgmv_
 KERNEL_SOURCES = {
     "decode_qkv": ("lora_small.cuh", "lora_small.cu") + _SHARED_SOURCES,
     "lm_head_decode": ("lora_small.cuh", "lora_small.cu") + _SHARED_SOURCES,
-    "prefill_gate_up": ("lora_ws.cuh", "lora_ws.cu", "lora_expand.cu") + _SHARED_SOURCES,
+    "prefill_gate_up": ("lora_stream.cuh", "lora_stream.cu", "lora_sshrink.cu") + _SHARED_SOURCES,
+    "skewed_down_proj": ("lora_stream.cuh", "lora_stream.cu", "lora_sshrink.cu") + _SHARED_SOURCES,
 }
 
 

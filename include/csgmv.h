@@ -218,21 +218,47 @@ CSGMV_API int csgmv_expand(const void *h, int h_dtype, int64_t ldh, const void *
  * csgmv_expand; base_output is bf16 (s, N), updated in place.
  *   workspace, workspace_bytes   optional device scratch for h (NULL / 0 for
  *       none).  Without it h never leaves the chip (reduced across a
- *       thread-block cluster in distributed shared memory).  With at least
- *       csgmv_qkv_workspace_bytes() bytes, two kinds of call may instead run
- *       the shrink and the expand as two kernels with fp32 h in the
- *       workspace, which is faster there: batches of long per-slot runs with
- *       K <= 4096 (prefill), and short per-slot runs with at least 32768
- *       output columns (a vocabulary-wide lm_head).  Its
- *       contents on entry do not matter; on return they are unspecified.  It
- *       must be 16-byte aligned and must not overlap any other argument.
+ *       thread-block cluster in distributed shared memory).  With room for
+ *       at least one plane of fp32 h (num_tokens * num_slices * max_rank * 4
+ *       bytes; csgmv_qkv_workspace_bytes() covers every batch and the widest
+ *       split of K), two kinds of call instead run the shrink and the expand
+ *       as two kernels with h in the workspace, which is faster there:
+ *       batches of long per-slot runs (128-token tiles, max_rank >= 16; the
+ *       shrink may cut K into parts, one plane of partial sums each, that the
+ *       expand adds in order), and short per-slot runs with at least 32768
+ *       output columns (a vocabulary-wide lm_head).  Its contents on entry do
+ *       not matter; on return they are unspecified.  It must be 16-byte
+ *       aligned and must not overlap any other argument.
  */
 CSGMV_API int csgmv_qkv(const void *x, int64_t K, const void *A, const void *B, int64_t N,
               const int32_t *slice_offsets, int num_slices, int max_slice_size, void *base_output,
               void *workspace, size_t workspace_bytes, const csgmv_batch_info *bi, csgmv_stream_t stream);
 
+/*
+ * Tuple-form B (base_backend.py run_qkv_lora: qkv_lora_b as a tuple of a q
+ * buffer (1, num_lora, output_dim_q, r) and a combined kv buffer
+ * (2, num_lora, output_dim_kv, r); run_gate_up_lora: gate_up_lora_b as a tuple
+ * of two (num_lora, output_dim, r) buffers).  These are csgmv_expand and
+ * csgmv_qkv with B given per slice instead of as one tensor:
+ *   B_slices  HOST array of num_slices device pointers; B_slices[j] is bf16
+ *             (max_loras, off[j+1] - off[j], R), row 0 being output column
+ *             off[j].  For the qkv tuple: {q, kv, kv + max_loras * N_kv * R}.
+ * Every slice offset must be a multiple of 64 (CSGMV_ERR_UNSUPPORTED
+ * otherwise); everything else, results included, is as the single-tensor call.
+ */
+CSGMV_API int csgmv_expand_sliced(const void *h, int h_dtype, int64_t ldh, const void *const *B_slices, int64_t N,
+                                  const int32_t *slice_offsets, int num_slices, int max_slice_size, void *out,
+                                  int accumulate, const csgmv_batch_info *bi, csgmv_stream_t stream);
+CSGMV_API int csgmv_qkv_sliced(const void *x, int64_t K, const void *A, const void *const *B_slices, int64_t N,
+                               const int32_t *slice_offsets, int num_slices, int max_slice_size, void *base_output,
+                               void *workspace, size_t workspace_bytes, const csgmv_batch_info *bi,
+                               csgmv_stream_t stream);
+
 /* Workspace bytes that let csgmv_qkv use its two-kernel path for any batch
- * of this batch info: max_tokens * num_slices * max_rank * 4 (fp32 h). */
+ * of this batch info, with h (fp32) held as up to four partial sums over parts
+ * of K: 4 * max_tokens * num_slices * max_rank * 4.  A smaller workspace of at
+ * least max_tokens * num_slices * max_rank * 4 bytes also takes the path, with
+ * fewer parts. */
 CSGMV_API size_t csgmv_qkv_workspace_bytes(const csgmv_batch_info *bi, int num_slices);
 
 /*
@@ -272,6 +298,46 @@ CSGMV_API int csgmv_qkv_static_scratch(const void *x, int64_t K, const void *A, 
  */
 CSGMV_API int embedding_lora_a(const int32_t *input_ids, const void *A_emb, int64_t vocab_size, int rank,
                      void *out, const csgmv_batch_info *bi, csgmv_stream_t stream);
+
+/*
+ * Embedding LoRA-A gather with extra tokens (base_backend.py
+ * run_lora_a_embedding with extra_embeddings: tokens with ids >= vocab_size
+ * are extra tokens the adapter adds beyond the base vocabulary).  For token t
+ * on slot w with rank r:
+ *     out[t][k] = A_emb[w][k][id]                    0 <= id < vocab_size
+ *     out[t][k] = extra_embeddings[w][id - vocab_size][k]
+ *                                 vocab_size <= id < vocab_size + num_extra_tokens
+ * for k < r, and 0 for r <= k < rank.
+ *   extra_embeddings  bf16 (max_loras, num_extra_tokens, rank); may be NULL
+ *                     when num_extra_tokens = 0 (then this is embedding_lora_a)
+ *   other arguments as embedding_lora_a; out must be 16-byte aligned when rank
+ *   is a multiple of 8.
+ * An id outside [0, vocab_size + num_extra_tokens) sets
+ * CSGMV_STATUS_BAD_TOKEN_ID and leaves that row 0.  Bit-exact copy.
+ */
+CSGMV_API int embedding_lora_a_extra(const int32_t *input_ids, const void *A_emb, int64_t vocab_size, int rank,
+                                     const void *extra_embeddings, int64_t num_extra_tokens, void *out,
+                                     const csgmv_batch_info *bi, csgmv_stream_t stream);
+
+/*
+ * Extra-token embedding (base_backend.py run_extra_token_embedding): in the
+ * (s, embed_dim) output of the base embedding, the row of every token t on
+ * slot w with vocab_size <= id < vocab_size + num_extra_tokens becomes
+ *     output[t][:] = extra_embeddings[w][id - vocab_size][:]
+ * (the base vocabulary has no row for it); rows of ids below vocab_size are
+ * not touched.
+ *   input_ids         int32 (s,), s = bi->num_tokens (tokens mapped to slots
+ *                     by the batch info)
+ *   output            bf16 (s, embed_dim), updated in place
+ *   extra_embeddings  bf16 (max_loras, num_extra_tokens, embed_dim)
+ * Both bf16 tensors must be 16-byte aligned when embed_dim is a multiple of
+ * 8.  An id outside [0, vocab_size + num_extra_tokens) sets
+ * CSGMV_STATUS_BAD_TOKEN_ID and leaves the row untouched; num_extra_tokens = 0
+ * does nothing.  Bit-exact copy.
+ */
+CSGMV_API int extra_token_embedding(const int32_t *input_ids, void *output, int64_t embed_dim,
+                                    const void *extra_embeddings, int64_t num_extra_tokens, int64_t vocab_size,
+                                    const csgmv_batch_info *bi, csgmv_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -23,7 +23,8 @@ STATUS_BITS = {
 
 EXPORTED = ["csgmv_last_error", "csgmv_version", "csgmv_chunk_size", "csgmv_batch_info_capacity",
             "csgmv_build_batch_info", "csgmv_build_lm_head_batch_info", "csgmv_shrink", "csgmv_expand", "csgmv_qkv", "csgmv_qkv_workspace_bytes",
-            "csgmv_qkv_static_scratch", "embedding_lora_a"]
+            "csgmv_qkv_static_scratch", "embedding_lora_a", "embedding_lora_a_extra", "extra_token_embedding",
+            "csgmv_expand_sliced", "csgmv_qkv_sliced"]
 
 
 class CsgmvError(RuntimeError):
@@ -69,6 +70,11 @@ def lib():
         "csgmv_qkv_workspace_bytes": (ctypes.c_size_t, [bip, i32]),
         "csgmv_qkv_static_scratch": (i32, [vp, i64, vp, vp, i64, i32p, i32, i32, vp, bip, vp]),
         "embedding_lora_a": (i32, [vp, vp, i64, i32, vp, bip, vp]),
+        "embedding_lora_a_extra": (i32, [vp, vp, i64, i32, vp, i64, vp, bip, vp]),
+        "csgmv_expand_sliced": (i32, [vp, i32, i64, ctypes.POINTER(vp), i64, i32p, i32, i32, vp, i32, bip, vp]),
+        "csgmv_qkv_sliced": (i32, [vp, i64, vp, ctypes.POINTER(vp), i64, i32p, i32, i32, vp, vp, ctypes.c_size_t,
+                                   bip, vp]),
+        "extra_token_embedding": (i32, [vp, vp, i64, vp, i64, i64, bip, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -244,3 +250,51 @@ def embedding_lora_a(input_ids: torch.Tensor, A_emb: torch.Tensor, vocab_size: i
     _check(lib().embedding_lora_a(_ptr(input_ids), _ptr(A_emb), int(vocab_size), rank, _ptr(out),
                                   ctypes.byref(bi.c), _stream(stream)))
     return out
+
+
+def embedding_lora_a_extra(input_ids: torch.Tensor, A_emb: torch.Tensor, vocab_size: int,
+                           extra_embeddings: torch.Tensor | None, out: torch.Tensor, bi: BatchInfo,
+                           stream=None) -> torch.Tensor:
+    """out (s, R) = LoRA-A rows of each token's id, from A_emb (L, R, V) for
+    ids below vocab_size and from extra_embeddings (L, E, R) above."""
+    E = 0 if extra_embeddings is None else int(extra_embeddings.shape[1])
+    _check(lib().embedding_lora_a_extra(_ptr(input_ids), _ptr(A_emb), int(vocab_size), int(out.shape[1]),
+                                        _ptr(extra_embeddings), E, _ptr(out), ctypes.byref(bi.c), _stream(stream)))
+    return out
+
+
+def extra_token_embedding(input_ids: torch.Tensor, output: torch.Tensor, extra_embeddings: torch.Tensor,
+                          vocab_size: int, bi: BatchInfo, stream=None) -> torch.Tensor:
+    """Rows of extra tokens (ids >= vocab_size) of output (s, D) become
+    extra_embeddings[slot][id - vocab_size]; other rows are untouched."""
+    _check(lib().extra_token_embedding(_ptr(input_ids), _ptr(output), int(output.shape[1]), _ptr(extra_embeddings),
+                                       int(extra_embeddings.shape[1]), int(vocab_size), ctypes.byref(bi.c),
+                                       _stream(stream)))
+    return output
+
+
+def _slice_ptrs(B_slices) -> ctypes.Array:
+    return (ctypes.c_void_p * len(B_slices))(*[t.data_ptr() for t in B_slices])
+
+
+def csgmv_expand_sliced(h: torch.Tensor, B_slices, slice_offsets, num_slices: int, max_slice_size: int,
+                        out: torch.Tensor, accumulate: bool, bi: BatchInfo, stream=None) -> torch.Tensor:
+    """csgmv_expand with B given per slice: B_slices[j] is (max_loras, off[j+1]-off[j], R)."""
+    dt = CSGMV_DTYPE_F32 if h.dtype == torch.float32 else CSGMV_DTYPE_BF16
+    _check(lib().csgmv_expand_sliced(_ptr(h), dt, int(h.stride(0)), _slice_ptrs(B_slices), int(out.shape[1]),
+                                     _offsets(slice_offsets), int(num_slices), int(max_slice_size), _ptr(out),
+                                     int(bool(accumulate)), ctypes.byref(bi.c), _stream(stream)))
+    return out
+
+
+def csgmv_qkv_sliced(x: torch.Tensor, A: torch.Tensor, B_slices, slice_offsets, num_slices: int,
+                     max_slice_size: int, base_output: torch.Tensor, bi: BatchInfo, workspace: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """csgmv_qkv with B given per slice (the tuple form of run_qkv_lora /
+    run_gate_up_lora): B_slices[j] is (max_loras, off[j+1]-off[j], R)."""
+    K = int(x.shape[1])
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().csgmv_qkv_sliced(_ptr(x), K, _ptr(A), _slice_ptrs(B_slices), int(base_output.shape[1]),
+                                  _offsets(slice_offsets), int(num_slices), int(max_slice_size), _ptr(base_output),
+                                  _ptr(workspace), ws_bytes, ctypes.byref(bi.c), _stream(stream)))
+    return base_output

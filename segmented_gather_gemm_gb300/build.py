@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libcsgmv.so")
 SOURCES = ["api.cu", "builder.cu", "embedding.cu", "lora_launch.cu", "lora_fused.cu", "lora_shrink.cu", "lora_expand.cu",
-           "lora_ws.cu", "lora_small.cu", "lora_stream.cu", "qkv_static.cu"]
+           "lora_small.cu", "lora_stream.cu", "lora_sshrink.cu", "qkv_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -60,7 +60,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, "-shared", "-o", tmp] + objs + ARCH
+    cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-Xlinker", "--no-undefined"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -1,6 +1,7 @@
 // C ABI of libcsgmv.so (declared in include/csgmv.h): argument checks on the
 // host, then one kernel launch per call on the caller's stream.  Nothing here
 // allocates, frees or synchronizes.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -109,6 +110,8 @@ void single_b(csgmv::LoraParams &p) {
 }
 
 void fill_common(csgmv::LoraParams &p, const csgmv_batch_info *bi) {
+    p.h_parts = 1;
+    p.h_plane = 0;
     p.seg_indptr = bi->seg_indptr;
     p.weight_indices = bi->weight_indices;
     p.permutation = bi->permutation;
@@ -120,6 +123,137 @@ void fill_common(csgmv::LoraParams &p, const csgmv_batch_info *bi) {
     p.num_tokens = bi->num_tokens;
     p.max_loras = bi->max_loras;
     p.R = bi->max_rank;
+}
+
+// B as one (max_loras, N, R) tensor, or as one (max_loras, off[j+1] - off[j], R)
+// tensor per slice (tuple form; slice offsets multiples of 64).
+int check_b(const void *B, const void *const *B_slices, const int32_t *off, int c) {
+    if (!B_slices) {
+        if (!B) return fail(CSGMV_ERR_INVALID_ARG, "B is NULL");
+        if (!aligned16(B)) return fail(CSGMV_ERR_INVALID_ARG, "B must be 16-byte aligned");
+        return CSGMV_OK;
+    }
+    for (int j = 0; j < c; ++j) {
+        if (!B_slices[j]) return fail(CSGMV_ERR_INVALID_ARG, "B_slices[%d] is NULL", j);
+        if (!aligned16(B_slices[j])) return fail(CSGMV_ERR_INVALID_ARG, "B_slices[%d] must be 16-byte aligned", j);
+    }
+    for (int j = 0; j <= c; ++j)
+        if (off[j] % 64)
+            return fail(CSGMV_ERR_UNSUPPORTED, "with separate slice tensors, slice_offsets[%d] = %d must be a multiple of 64",
+                        j, off[j]);
+    return CSGMV_OK;
+}
+
+void set_b(csgmv::LoraParams &p, const void *const *B_slices) {
+    if (!B_slices) {
+        single_b(p);
+        p.b_tuple = 0;
+        return;
+    }
+    p.B = nullptr;
+    for (int j = 0; j < csgmv::kMaxSlices; ++j) {
+        const int jj = j < p.c ? j : 0;
+        p.Bs[j] = static_cast<const uint16_t *>(B_slices[jj]);
+        p.b_rows[j] = p.off[jj + 1] - p.off[jj];
+        p.b_row0[j] = 0;
+    }
+    p.b_tuple = 1;
+}
+
+int expand_impl(const void *h, int h_dtype, int64_t ldh, const void *B, const void *const *B_slices, int64_t N,
+                const int32_t *slice_offsets, int num_slices, int max_slice_size, void *out, int accumulate,
+                const csgmv_batch_info *bi, csgmv_stream_t stream) {
+    int rc = check_bi(bi, true);
+    if (rc) return rc;
+    if ((rc = check_rank(bi))) return rc;
+    if ((rc = check_offsets(slice_offsets, num_slices, N, max_slice_size))) return rc;
+    if (N <= 0 || N % 8 != 0 || N > INT32_MAX) return fail(CSGMV_ERR_INVALID_ARG, "N %lld must be a positive multiple of 8", (long long)N);
+    if (h_dtype != CSGMV_DTYPE_BF16 && h_dtype != CSGMV_DTYPE_F32) return fail(CSGMV_ERR_INVALID_ARG, "bad h_dtype");
+    if (ldh < (int64_t)num_slices * bi->max_rank) return fail(CSGMV_ERR_INVALID_ARG, "ldh below c*R");
+    const int64_t s = bi->num_tokens;
+    if (s == 0) return CSGMV_OK;
+    if (!h || !out) return fail(CSGMV_ERR_INVALID_ARG, "NULL tensor");
+    if (!aligned16(out)) return fail(CSGMV_ERR_INVALID_ARG, "out must be 16-byte aligned");
+    if ((rc = check_b(B, B_slices, slice_offsets, num_slices))) return rc;
+    if (overlaps_batch_info(bi, out, (size_t)s * N * 2)) return fail(CSGMV_ERR_INVALID_ARG, "out overlaps the batch info");
+    csgmv::LoraParams p = {};
+    fill_common(p, bi);
+    p.B = static_cast<const uint16_t *>(B);
+    p.y = static_cast<uint16_t *>(out);
+    p.h = const_cast<void *>(h);
+    p.h_f32 = h_dtype == CSGMV_DTYPE_F32;
+    p.ldh = ldh;
+    p.N = N;
+    p.c = num_slices;
+    for (int j = 0; j <= num_slices; ++j) p.off[j] = slice_offsets[j];
+    set_b(p, B_slices);
+    p.accumulate = accumulate ? 1 : 0;
+    cudaError_t e = csgmv::launch_lora(csgmv::kModeExpand, p, *bi, reinterpret_cast<cudaStream_t>(stream), nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "csgmv_expand launch");
+    return CSGMV_OK;
+}
+
+int qkv_impl(const void *x, int64_t K, const void *A, const void *B, const void *const *B_slices, int64_t N,
+             const int32_t *slice_offsets, int num_slices, int max_slice_size, void *base_output, void *workspace,
+             size_t workspace_bytes, const csgmv_batch_info *bi, csgmv_stream_t stream) {
+    int rc = check_bi(bi, true);
+    if (rc) return rc;
+    if ((rc = check_rank(bi))) return rc;
+    if ((rc = check_offsets(slice_offsets, num_slices, N, max_slice_size))) return rc;
+    if (K <= 0 || K % 8 != 0 || K > INT32_MAX) return fail(CSGMV_ERR_INVALID_ARG, "K %lld must be a positive multiple of 8", (long long)K);
+    if (N <= 0 || N % 8 != 0 || N > INT32_MAX) return fail(CSGMV_ERR_INVALID_ARG, "N %lld must be a positive multiple of 8", (long long)N);
+    const int64_t s = bi->num_tokens;
+    if (s == 0) return CSGMV_OK;
+    if (!x || !A || !base_output) return fail(CSGMV_ERR_INVALID_ARG, "NULL tensor");
+    if (!aligned16(x) || !aligned16(A) || !aligned16(base_output))
+        return fail(CSGMV_ERR_INVALID_ARG, "x / A / base_output must be 16-byte aligned");
+    if ((rc = check_b(B, B_slices, slice_offsets, num_slices))) return rc;
+    if (overlaps_batch_info(bi, base_output, (size_t)s * N * 2))
+        return fail(CSGMV_ERR_INVALID_ARG, "base_output overlaps the batch info");
+    csgmv::LoraParams p = {};
+    fill_common(p, bi);
+    p.x = static_cast<const uint16_t *>(x);
+    p.A = static_cast<const uint16_t *>(A);
+    p.B = static_cast<const uint16_t *>(B);
+    p.y = static_cast<uint16_t *>(base_output);
+    p.K = K;
+    p.N = N;
+    p.c = num_slices;
+    for (int j = 0; j <= num_slices; ++j) p.off[j] = slice_offsets[j];
+    set_b(p, B_slices);
+    p.accumulate = 1;
+    const size_t hbytes = (size_t)s * num_slices * bi->max_rank * 4;
+    if (workspace && workspace_bytes >= hbytes && csgmv::qkv_split_pays(p, *bi)) {
+        // the planes of h the call may write: up to kMaxKParts of hbytes
+        const size_t ws_used = std::min(workspace_bytes, (size_t)csgmv::kMaxKParts * hbytes);
+        if (!aligned16(workspace)) return fail(CSGMV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+        if (overlaps_batch_info(bi, workspace, ws_used) ||
+            overlaps(workspace, ws_used, base_output, (size_t)s * N * 2))
+            return fail(CSGMV_ERR_INVALID_ARG, "workspace overlaps the batch info or base_output");
+        // shrink into the workspace (fp32 h, columns [0, c*R), one plane per
+        // part of K), then expand onto base_output
+        csgmv::LoraParams ps = p;
+        ps.B = nullptr;
+        ps.y = nullptr;
+        ps.N = 0;
+        ps.h = workspace;
+        ps.h_f32 = 1;
+        ps.ldh = (int64_t)num_slices * bi->max_rank;
+        ps.accumulate = 0;
+        csgmv::LoraParams pe = p;
+        pe.x = nullptr;
+        pe.A = nullptr;
+        pe.K = 0;
+        pe.h = workspace;
+        pe.h_f32 = 1;
+        pe.ldh = ps.ldh;
+        cudaError_t e = csgmv::launch_qkv_split(ps, pe, *bi, reinterpret_cast<cudaStream_t>(stream), ws_used);
+        if (e != cudaSuccess) return cuda_fail(e, "csgmv_qkv shrink / expand launch");
+        return CSGMV_OK;
+    }
+    cudaError_t e = csgmv::launch_lora(csgmv::kModeFused, p, *bi, reinterpret_cast<cudaStream_t>(stream), nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "csgmv_qkv launch");
+    return CSGMV_OK;
 }
 
 }  // namespace
@@ -265,121 +399,103 @@ int csgmv_shrink(const void *x, int64_t s, int64_t K, const void *A, int num_sli
 int csgmv_expand(const void *h, int h_dtype, int64_t ldh, const void *B, int64_t N, const int32_t *slice_offsets,
                  int num_slices, int max_slice_size, void *out, int accumulate, const csgmv_batch_info *bi,
                  csgmv_stream_t stream) {
-    int rc = check_bi(bi, true);
-    if (rc) return rc;
-    if ((rc = check_rank(bi))) return rc;
-    if ((rc = check_offsets(slice_offsets, num_slices, N, max_slice_size))) return rc;
-    if (N <= 0 || N % 8 != 0 || N > INT32_MAX) return fail(CSGMV_ERR_INVALID_ARG, "N %lld must be a positive multiple of 8", (long long)N);
-    if (h_dtype != CSGMV_DTYPE_BF16 && h_dtype != CSGMV_DTYPE_F32) return fail(CSGMV_ERR_INVALID_ARG, "bad h_dtype");
-    if (ldh < (int64_t)num_slices * bi->max_rank) return fail(CSGMV_ERR_INVALID_ARG, "ldh below c*R");
-    const int64_t s = bi->num_tokens;
-    if (s == 0) return CSGMV_OK;
-    if (!h || !B || !out) return fail(CSGMV_ERR_INVALID_ARG, "NULL tensor");
-    if (!aligned16(B) || !aligned16(out)) return fail(CSGMV_ERR_INVALID_ARG, "B / out must be 16-byte aligned");
-    if (overlaps_batch_info(bi, out, (size_t)s * N * 2)) return fail(CSGMV_ERR_INVALID_ARG, "out overlaps the batch info");
-    csgmv::LoraParams p = {};
-    fill_common(p, bi);
-    p.B = static_cast<const uint16_t *>(B);
-    p.y = static_cast<uint16_t *>(out);
-    p.h = const_cast<void *>(h);
-    p.h_f32 = h_dtype == CSGMV_DTYPE_F32;
-    p.ldh = ldh;
-    p.N = N;
-    p.c = num_slices;
-    for (int j = 0; j <= num_slices; ++j) p.off[j] = slice_offsets[j];
-    single_b(p);
-    p.accumulate = accumulate ? 1 : 0;
-    cudaError_t e = csgmv::launch_lora(csgmv::kModeExpand, p, *bi, reinterpret_cast<cudaStream_t>(stream), nullptr);
-    if (e != cudaSuccess) return cuda_fail(e, "csgmv_expand launch");
-    return CSGMV_OK;
+    return expand_impl(h, h_dtype, ldh, B, nullptr, N, slice_offsets, num_slices, max_slice_size, out, accumulate,
+                       bi, stream);
+}
+
+int csgmv_expand_sliced(const void *h, int h_dtype, int64_t ldh, const void *const *B_slices, int64_t N,
+                        const int32_t *slice_offsets, int num_slices, int max_slice_size, void *out, int accumulate,
+                        const csgmv_batch_info *bi, csgmv_stream_t stream) {
+    if (!B_slices) return fail(CSGMV_ERR_INVALID_ARG, "B_slices is NULL");
+    return expand_impl(h, h_dtype, ldh, nullptr, B_slices, N, slice_offsets, num_slices, max_slice_size, out,
+                       accumulate, bi, stream);
 }
 
 size_t csgmv_qkv_workspace_bytes(const csgmv_batch_info *bi, int num_slices) {
     if (!bi || bi->max_tokens < 0 || bi->max_rank < 0 || num_slices < 1 || num_slices > csgmv::kMaxSlices) return 0;
-    return (size_t)bi->max_tokens * num_slices * bi->max_rank * 4;
+    return (size_t)csgmv::kMaxKParts * bi->max_tokens * num_slices * bi->max_rank * 4;
 }
 
 int csgmv_qkv(const void *x, int64_t K, const void *A, const void *B, int64_t N, const int32_t *slice_offsets,
               int num_slices, int max_slice_size, void *base_output, void *workspace, size_t workspace_bytes,
               const csgmv_batch_info *bi, csgmv_stream_t stream) {
-    int rc = check_bi(bi, true);
-    if (rc) return rc;
-    if ((rc = check_rank(bi))) return rc;
-    if ((rc = check_offsets(slice_offsets, num_slices, N, max_slice_size))) return rc;
-    if (K <= 0 || K % 8 != 0 || K > INT32_MAX) return fail(CSGMV_ERR_INVALID_ARG, "K %lld must be a positive multiple of 8", (long long)K);
-    if (N <= 0 || N % 8 != 0 || N > INT32_MAX) return fail(CSGMV_ERR_INVALID_ARG, "N %lld must be a positive multiple of 8", (long long)N);
-    const int64_t s = bi->num_tokens;
-    if (s == 0) return CSGMV_OK;
-    if (!x || !A || !B || !base_output) return fail(CSGMV_ERR_INVALID_ARG, "NULL tensor");
-    if (!aligned16(x) || !aligned16(A) || !aligned16(B) || !aligned16(base_output))
-        return fail(CSGMV_ERR_INVALID_ARG, "x / A / B / base_output must be 16-byte aligned");
-    if (overlaps_batch_info(bi, base_output, (size_t)s * N * 2))
-        return fail(CSGMV_ERR_INVALID_ARG, "base_output overlaps the batch info");
-    csgmv::LoraParams p = {};
-    fill_common(p, bi);
-    p.x = static_cast<const uint16_t *>(x);
-    p.A = static_cast<const uint16_t *>(A);
-    p.B = static_cast<const uint16_t *>(B);
-    p.y = static_cast<uint16_t *>(base_output);
-    p.K = K;
-    p.N = N;
-    p.c = num_slices;
-    for (int j = 0; j <= num_slices; ++j) p.off[j] = slice_offsets[j];
-    single_b(p);
-    p.accumulate = 1;
-    const size_t hbytes = (size_t)s * num_slices * bi->max_rank * 4;
-    if (workspace && workspace_bytes >= hbytes && csgmv::qkv_split_pays(p, *bi)) {
-        if (!aligned16(workspace)) return fail(CSGMV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-        if (overlaps_batch_info(bi, workspace, hbytes) ||
-            overlaps(workspace, hbytes, base_output, (size_t)s * N * 2))
-            return fail(CSGMV_ERR_INVALID_ARG, "workspace overlaps the batch info or base_output");
-        // shrink into the workspace (fp32 h, columns [0, c*R)), then expand onto base_output
-        csgmv::LoraParams ps = p;
-        ps.B = nullptr;
-        ps.y = nullptr;
-        ps.N = 0;
-        ps.h = workspace;
-        ps.h_f32 = 1;
-        ps.ldh = (int64_t)num_slices * bi->max_rank;
-        ps.accumulate = 0;
-        cudaError_t e = csgmv::launch_lora(csgmv::kModeShrink, ps, *bi, reinterpret_cast<cudaStream_t>(stream), nullptr);
-        if (e != cudaSuccess) return cuda_fail(e, "csgmv_qkv shrink launch");
-        csgmv::LoraParams pe = p;
-        pe.x = nullptr;
-        pe.A = nullptr;
-        pe.K = 0;
-        pe.h = workspace;
-        pe.h_f32 = 1;
-        pe.ldh = ps.ldh;
-        e = csgmv::launch_lora(csgmv::kModeExpand, pe, *bi, reinterpret_cast<cudaStream_t>(stream), nullptr);
-        if (e != cudaSuccess) return cuda_fail(e, "csgmv_qkv expand launch");
-        return CSGMV_OK;
-    }
-    cudaError_t e = csgmv::launch_lora(csgmv::kModeFused, p, *bi, reinterpret_cast<cudaStream_t>(stream), nullptr);
-    if (e != cudaSuccess) return cuda_fail(e, "csgmv_qkv launch");
-    return CSGMV_OK;
+    return qkv_impl(x, K, A, B, nullptr, N, slice_offsets, num_slices, max_slice_size, base_output, workspace,
+                    workspace_bytes, bi, stream);
+}
+
+int csgmv_qkv_sliced(const void *x, int64_t K, const void *A, const void *const *B_slices, int64_t N,
+                     const int32_t *slice_offsets, int num_slices, int max_slice_size, void *base_output,
+                     void *workspace, size_t workspace_bytes, const csgmv_batch_info *bi, csgmv_stream_t stream) {
+    if (!B_slices) return fail(CSGMV_ERR_INVALID_ARG, "B_slices is NULL");
+    return qkv_impl(x, K, A, nullptr, B_slices, N, slice_offsets, num_slices, max_slice_size, base_output, workspace,
+                    workspace_bytes, bi, stream);
 }
 
 int embedding_lora_a(const int32_t *input_ids, const void *A_emb, int64_t vocab_size, int rank, void *out,
                      const csgmv_batch_info *bi, csgmv_stream_t stream) {
+    return embedding_lora_a_extra(input_ids, A_emb, vocab_size, rank, nullptr, 0, out, bi, stream);
+}
+
+int embedding_lora_a_extra(const int32_t *input_ids, const void *A_emb, int64_t vocab_size, int rank,
+                           const void *extra_embeddings, int64_t num_extra_tokens, void *out,
+                           const csgmv_batch_info *bi, csgmv_stream_t stream) {
     int rc = check_bi(bi, true);
     if (rc) return rc;
     if (rank < 1 || rank > 1024) return fail(CSGMV_ERR_UNSUPPORTED, "rank %d not in [1, 1024]", rank);
     if (vocab_size <= 0) return fail(CSGMV_ERR_INVALID_ARG, "vocab_size must be positive");
+    if (num_extra_tokens < 0) return fail(CSGMV_ERR_INVALID_ARG, "num_extra_tokens must be non-negative");
+    if (num_extra_tokens > 0 && !extra_embeddings)
+        return fail(CSGMV_ERR_INVALID_ARG, "extra_embeddings is NULL with num_extra_tokens > 0");
+    if (vocab_size + num_extra_tokens > INT32_MAX)
+        return fail(CSGMV_ERR_INVALID_ARG, "vocab_size + num_extra_tokens exceeds int32 token ids");
     const int64_t s = bi->num_tokens;
     if (s == 0) return CSGMV_OK;
     if (!input_ids || !A_emb || !out) return fail(CSGMV_ERR_INVALID_ARG, "NULL tensor");
+    if (rank % 8 == 0 && !aligned16(out)) return fail(CSGMV_ERR_INVALID_ARG, "out must be 16-byte aligned");
     if (overlaps_batch_info(bi, out, (size_t)s * rank * 2)) return fail(CSGMV_ERR_INVALID_ARG, "out overlaps the batch info");
     csgmv::EmbeddingParams p;
     p.ids = input_ids;
     p.A = static_cast<const uint16_t *>(A_emb);
+    p.extra = num_extra_tokens > 0 ? static_cast<const uint16_t *>(extra_embeddings) : nullptr;
     p.out = static_cast<uint16_t *>(out);
     p.V = vocab_size;
+    p.E = num_extra_tokens > 0 ? num_extra_tokens : 0;
     p.R = rank;
     p.num_tokens = bi->num_tokens;
     p.max_loras = bi->max_loras;
     cudaError_t e = csgmv::launch_embedding(p, *bi, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "embedding_lora_a launch");
+    return CSGMV_OK;
+}
+
+int extra_token_embedding(const int32_t *input_ids, void *output, int64_t embed_dim, const void *extra_embeddings,
+                          int64_t num_extra_tokens, int64_t vocab_size, const csgmv_batch_info *bi,
+                          csgmv_stream_t stream) {
+    int rc = check_bi(bi, true);
+    if (rc) return rc;
+    if (embed_dim <= 0) return fail(CSGMV_ERR_INVALID_ARG, "embed_dim must be positive");
+    if (vocab_size <= 0) return fail(CSGMV_ERR_INVALID_ARG, "vocab_size must be positive");
+    if (num_extra_tokens < 0) return fail(CSGMV_ERR_INVALID_ARG, "num_extra_tokens must be non-negative");
+    if (vocab_size + num_extra_tokens > INT32_MAX)
+        return fail(CSGMV_ERR_INVALID_ARG, "vocab_size + num_extra_tokens exceeds int32 token ids");
+    const int64_t s = bi->num_tokens;
+    if (s == 0 || num_extra_tokens == 0) return CSGMV_OK;
+    if (!input_ids || !output || !extra_embeddings) return fail(CSGMV_ERR_INVALID_ARG, "NULL tensor");
+    if (embed_dim % 8 == 0 && (!aligned16(output) || !aligned16(extra_embeddings)))
+        return fail(CSGMV_ERR_INVALID_ARG, "output / extra_embeddings must be 16-byte aligned");
+    if (overlaps_batch_info(bi, output, (size_t)s * embed_dim * 2))
+        return fail(CSGMV_ERR_INVALID_ARG, "output overlaps the batch info");
+    csgmv::ExtraTokenParams p;
+    p.ids = input_ids;
+    p.extra = static_cast<const uint16_t *>(extra_embeddings);
+    p.out = static_cast<uint16_t *>(output);
+    p.V = vocab_size;
+    p.E = num_extra_tokens;
+    p.D = embed_dim;
+    p.num_tokens = bi->num_tokens;
+    p.max_loras = bi->max_loras;
+    cudaError_t e = csgmv::launch_extra_token(p, *bi, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "extra_token_embedding launch");
     return CSGMV_OK;
 }
 

@@ -11,6 +11,7 @@ constexpr int kMinChunkSize = 16;  // chunked_backend.py MIN_CHUNK_SIZE
 constexpr int kMaxRank = 64;       // largest buffer rank R the LoRA kernels take
 constexpr int kMaxSlices = 3;
 constexpr int kWideCols = 32768;   // output columns from which 16- / 32-token csgmv_qkv calls split
+constexpr int kMaxKParts = 4;      // fp32 h planes of the csgmv_qkv workspace (parts of K)
 
 #ifdef __CUDACC__
 // Programmatic dependent launch.  A kernel launched with
@@ -40,9 +41,14 @@ struct LoraParams {
     // tensor is Bs[j] = B, b_rows[j] = N, b_row0[j] = off[j].
     const uint16_t *Bs[kMaxSlices];
     int b_rows[kMaxSlices], b_row0[kMaxSlices];
+    int b_tuple;         // 1: the slices are separate tensors (slice offsets multiples of 64)
     uint16_t *y;         // (s, N) bf16, in/out
     void *h;             // (s, ldh) bf16 or f32 (shrink output / expand input)
     int64_t K, N, ldh;
+    // fp32 h held as h_parts partial sums over parts of K, h_plane elements
+    // apart (the csgmv_qkv workspace path); 1 = h itself
+    int h_parts;
+    int64_t h_plane;
     int h_f32;
     int c, R;
     int off[kMaxSlices + 1];
@@ -78,6 +84,11 @@ int set_error(int code, const char *msg);
 
 // Whether csgmv_qkv should run as shrink + expand through a workspace.
 bool qkv_split_pays(const LoraParams &p, const csgmv_batch_info &bi);
+// csgmv_qkv's two-kernel path: shrink (ps) into the fp32 workspace, as up to
+// workspace_bytes / (s * c * R * 4) partial-sum planes over parts of K, then
+// the expand (pe) from it.
+cudaError_t launch_qkv_split(LoraParams &ps, LoraParams &pe, const csgmv_batch_info &bi, cudaStream_t stream,
+                             size_t workspace_bytes);
 
 // builder.cu
 struct BuildParams {
@@ -94,12 +105,21 @@ cudaError_t launch_build_lm_head(const BuildParams &p, const csgmv_batch_info &b
 // embedding.cu
 struct EmbeddingParams {
     const int32_t *ids;
-    const uint16_t *A;
-    uint16_t *out;
-    int64_t V;
+    const uint16_t *A;      // (max_loras, R, V)
+    const uint16_t *extra;  // (max_loras, E, R) rows of extra tokens, or NULL (E = 0)
+    uint16_t *out;          // (s, R)
+    int64_t V, E;
     int R;
     int num_tokens, max_loras;
 };
 cudaError_t launch_embedding(const EmbeddingParams &p, const csgmv_batch_info &bi, cudaStream_t stream);
+struct ExtraTokenParams {
+    const int32_t *ids;
+    const uint16_t *extra;  // (max_loras, E, D)
+    uint16_t *out;          // (s, D), rows of extra tokens overwritten
+    int64_t V, E, D;
+    int num_tokens, max_loras;
+};
+cudaError_t launch_extra_token(const ExtraTokenParams &p, const csgmv_batch_info &bi, cudaStream_t stream);
 
 }  // namespace csgmv

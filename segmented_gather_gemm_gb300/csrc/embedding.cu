@@ -1,64 +1,88 @@
-// Embedding LoRA-A gather (sglang base_backend.py run_lora_a_embedding;
-// chunked_backend.py run_lora_a_embedding, no extra-token embeddings):
-//     out[t][k] = A_emb[w(t)][k][ids[t]]   k < r_w,   0 for r_w <= k < R.
-// A_emb is (L, R, V), so the R values of one token are V elements apart: each
-// is its own 32-byte sector and the gather is bound by sector count and
-// latency, not by bytes.  Blocks own (segment, token-slice) pairs so the slot
-// is read once per segment; each warp takes one token row at a time with one
-// lane per rank column (so the output row is one coalesced store), and every
-// lane issues its loads for four tokens before storing, to keep several
-// sectors in flight per lane.
+// Embedding LoRA-A gather and extra-token embedding (sglang base_backend.py
+// run_lora_a_embedding with optional extra_embeddings, and
+// run_extra_token_embedding; chunked_backend.py run_lora_a_embedding):
+//     out[t][k] = A_emb[w(t)][k][id]            0 <= id < V,      k < r_w
+//     out[t][k] = extra[w(t)][id - V][k]        V <= id < V + E,  k < r_w
+//     out[t][k] = 0                             r_w <= k < R
+// A_emb is (L, R, V), so the R values of one token are V elements apart:
+// each is its own 32-byte sector, and the gather is bound by the number of
+// sectors in flight and by the chain of dependent loads (segment -> token ->
+// id -> table), not by bytes.  Blocks own (segment, token-slice) pairs so the
+// slot is read once per segment.
+#include <algorithm>
+
 #include "csgmv_internal.h"
 
 namespace csgmv {
 namespace {
 
-constexpr int kEmbThreads = 256;
-constexpr int kTokPerIter = 8;  // token rows per block iteration (32 lanes each)
-constexpr int kUnroll = 4;
+constexpr int kEmbThreads = 128;
+constexpr int kEmbWarps = kEmbThreads / 32;
+
+struct SegInfo {
+    int w, r, p0, p1;
+    bool ok;
+};
+
+// Segment seg of the batch info, its slot and rank (errors reported by one thread).
+__device__ __forceinline__ SegInfo seg_info(int seg, int num_tokens, int max_loras, int R,
+                                            const int32_t *seg_indptr, const int32_t *weight_indices,
+                                            const int32_t *ranks, int32_t *status, bool report) {
+    SegInfo g;
+    g.w = weight_indices[seg];
+    g.p0 = max(seg_indptr[seg], 0);
+    g.p1 = min(seg_indptr[seg + 1], num_tokens);
+    g.ok = g.w >= 0 && g.w < max_loras;
+    g.r = 0;
+    if (!g.ok) {
+        if (report) atomicOr(status, CSGMV_STATUS_BAD_ADAPTER);
+        return g;
+    }
+    g.r = ranks[g.w];
+    if (g.r < 0 || g.r > R) {
+        if (report) atomicOr(status, CSGMV_STATUS_BAD_RANK);
+        g.r = 0;
+    }
+    return g;
+}
+
+// One token row per warp at a time, one lane per rank column (the output row
+// is one coalesced store); every lane issues its loads for kUnroll tokens
+// before it stores, to keep that many sectors in flight per lane.
+constexpr int kTokPerIter = kEmbWarps;  // token rows per block iteration
+constexpr int kUnroll = 8;
 
 __global__ void __launch_bounds__(kEmbThreads)
 embedding_lora_a_kernel(EmbeddingParams p, const int32_t *__restrict__ seg_indptr,
                         const int32_t *__restrict__ weight_indices, const int32_t *__restrict__ permutation,
-                        const int32_t *__restrict__ ranks, const int32_t *__restrict__ nseg_dev,
-                        int32_t *status) {
+                        const int32_t *__restrict__ ranks, const int32_t *__restrict__ nseg_dev, int32_t *status) {
     griddep_wait();  // the batch info may come from the kernel launched just before
     const int nseg = *nseg_dev;
     const int ty = threadIdx.x >> 5, tx = threadIdx.x & 31;
     for (int seg = blockIdx.x; seg < nseg; seg += gridDim.x) {
-        const int w = weight_indices[seg];
-        const int p0 = max(seg_indptr[seg], 0), p1 = min(seg_indptr[seg + 1], p.num_tokens);
-        int r = 0;
-        const bool wok = w >= 0 && w < p.max_loras;
-        if (!wok) {
-            if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(status, CSGMV_STATUS_BAD_ADAPTER);
-        } else {
-            r = ranks[w];
-            if (r < 0 || r > p.R) {
-                if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(status, CSGMV_STATUS_BAD_RANK);
-                r = 0;
-            }
-        }
-        const uint16_t *Aw = p.A + (int64_t)(wok ? w : 0) * p.R * p.V;
+        const SegInfo g = seg_info(seg, p.num_tokens, p.max_loras, p.R, seg_indptr, weight_indices, ranks, status,
+                                   threadIdx.x == 0 && blockIdx.y == 0);
+        const uint16_t *Aw = p.A + (int64_t)(g.ok ? g.w : 0) * p.R * p.V;
+        const uint16_t *Ew = p.extra ? p.extra + (int64_t)(g.ok ? g.w : 0) * p.E * p.R : nullptr;
         const int step = gridDim.y * kTokPerIter;
-        for (int pb = p0 + blockIdx.y * kTokPerIter * kUnroll; pb < p1; pb += step * kUnroll) {
+        for (int pb = g.p0 + blockIdx.y * kTokPerIter * kUnroll; pb < g.p1; pb += step * kUnroll) {
             int t[kUnroll];
             int64_t id[kUnroll];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
-                int pos = pb + u * kTokPerIter + ty;
+                const int pos = pb + u * kTokPerIter + ty;
                 t[u] = -1;
                 id[u] = -1;
-                if (pos < p1) {
-                    int tt = permutation[pos];
+                if (pos < g.p1) {
+                    const int tt = permutation[pos];
                     if (tt < 0 || tt >= p.num_tokens) {
                         if (tx == 0) atomicOr(status, CSGMV_STATUS_BAD_PERMUTATION);
                     } else {
                         t[u] = tt;
-                        int64_t v = p.ids[tt];
-                        if (v < 0 || v >= p.V) {
+                        const int64_t v = p.ids[tt];
+                        if (v < 0 || v >= p.V + p.E) {
                             if (tx == 0) atomicOr(status, CSGMV_STATUS_BAD_TOKEN_ID);
-                        } else {
+                        } else if (g.ok) {
                             id[u] = v;
                         }
                     }
@@ -68,14 +92,93 @@ embedding_lora_a_kernel(EmbeddingParams p, const int32_t *__restrict__ seg_indpt
                 const int k = k0 + tx;
                 uint16_t v[kUnroll];
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u)
-                    v[u] = (id[u] >= 0 && k < r) ? __ldg(Aw + (int64_t)k * p.V + id[u]) : (uint16_t)0;
+                for (int u = 0; u < kUnroll; ++u) {
+                    v[u] = 0;
+                    if (id[u] >= 0 && k < g.r)
+                        v[u] = id[u] < p.V ? __ldg(Aw + (int64_t)k * p.V + id[u]) : __ldg(Ew + (id[u] - p.V) * p.R + k);
+                }
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u)
                     if (t[u] >= 0 && k < p.R) p.out[(int64_t)t[u] * p.R + k] = v[u];
             }
         }
     }
+}
+
+// Rows of extra tokens of an (s, D) output become extra[w][id - V][:].  Each
+// lane checks one token of the warp's slice; the warp then copies the rows of
+// the lanes that hold an extra token, one row at a time, 16 bytes per lane.
+__global__ void __launch_bounds__(kEmbThreads)
+extra_token_kernel(ExtraTokenParams p, const int32_t *__restrict__ seg_indptr,
+                   const int32_t *__restrict__ weight_indices, const int32_t *__restrict__ permutation,
+                   const int32_t *__restrict__ nseg_dev, int32_t *status, int spp) {
+    griddep_wait();
+    const int nseg = *nseg_dev;
+    const int lane = threadIdx.x & 31;
+    const int64_t nitems = (int64_t)max(nseg, 0) * spp;
+    const int64_t wstride = (int64_t)gridDim.x * kEmbWarps;
+    const bool vec = (p.D & 7) == 0;
+    for (int64_t it = (int64_t)blockIdx.x * kEmbWarps + (threadIdx.x >> 5); it < nitems; it += wstride) {
+        const int seg = (int)(it / spp), sl = (int)(it % spp);
+        const int w = weight_indices[seg];
+        const int p0 = max(seg_indptr[seg], 0), p1 = min(seg_indptr[seg + 1], p.num_tokens);
+        if (p0 + 32 * sl >= p1) continue;
+        const bool wok = w >= 0 && w < p.max_loras;
+        if (!wok && sl == 0 && lane == 0) atomicOr(status, CSGMV_STATUS_BAD_ADAPTER);
+        const int pos = p0 + 32 * sl + lane;
+        int t = -1;
+        int64_t e = -1;
+        if (pos < p1) {
+            const int tt = permutation[pos];
+            if (tt < 0 || tt >= p.num_tokens) {
+                atomicOr(status, CSGMV_STATUS_BAD_PERMUTATION);
+            } else {
+                const int64_t v = p.ids[tt];
+                if (v < 0 || v >= p.V + p.E) atomicOr(status, CSGMV_STATUS_BAD_TOKEN_ID);
+                else if (v >= p.V && wok) { t = tt; e = v - p.V; }
+            }
+        }
+        uint32_t todo = __ballot_sync(0xffffffffu, t >= 0);
+        while (todo) {
+            const int src = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const int tt = __shfl_sync(0xffffffffu, t, src);
+            const int64_t ee = __shfl_sync(0xffffffffu, e, src);
+            const uint16_t *from = p.extra + ((int64_t)w * p.E + ee) * p.D;
+            uint16_t *to = p.out + (int64_t)tt * p.D;
+            if (vec) {
+                for (int64_t d = 8 * lane; d < p.D; d += 256)
+                    *reinterpret_cast<uint4 *>(to + d) = __ldg(reinterpret_cast<const uint4 *>(from + d));
+            } else {
+                for (int64_t d = lane; d < p.D; d += 32) to[d] = __ldg(from + d);
+            }
+        }
+    }
+}
+
+// Grid for warps walking (segment, 32-token slice) items: enough blocks for
+// the largest batch the batch info holds, at most eight per SM.
+int item_grid(const csgmv_batch_info &bi, int spp) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t items = (int64_t)std::max(bi.max_segments, 1) * spp;
+    const int64_t blocks = (items + kEmbWarps - 1) / kEmbWarps;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)sms * 8));
+}
+
+cudaLaunchConfig_t item_config(const csgmv_batch_info &bi, int spp, cudaStream_t stream, cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(item_grid(bi, spp), 1, 1);
+    cfg.blockDim = dim3(kEmbThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    // programmatic dependent launch: the blocks start while the batch-info
+    // builder before them finishes, and wait for it on the device
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
 }
 
 }  // namespace
@@ -87,23 +190,25 @@ cudaError_t launch_embedding(const EmbeddingParams &p, const csgmv_batch_info &b
     int gy = (chunk + kTokPerIter * kUnroll - 1) / (kTokPerIter * kUnroll);
     gy = gy < 1 ? 1 : (gy > 64 ? 64 : gy);
     const int gx = bi.max_segments < 1 ? 1 : bi.max_segments;
-    dim3 grid(gx, gy, 1);
-    // programmatic dependent launch: the blocks start while the batch-info
-    // builder before it finishes, and wait for it on the device
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kEmbThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cudaLaunchConfig_t cfg = item_config(bi, 1, stream, attr);
+    cfg.gridDim = dim3(gx, gy, 1);
     cudaError_t e = cudaLaunchKernelEx(&cfg, embedding_lora_a_kernel, p, (const int32_t *)bi.seg_indptr,
                                        (const int32_t *)bi.weight_indices, (const int32_t *)bi.permutation,
                                        (const int32_t *)bi.lora_ranks, (const int32_t *)bi.num_segments_dev,
                                        (int32_t *)bi.status);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_extra_token(const ExtraTokenParams &p, const csgmv_batch_info &bi, cudaStream_t stream) {
+    const int chunk = bi.chunk_size > 0 ? bi.chunk_size : kMinChunkSize;
+    const int spp = (chunk + 31) / 32;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = item_config(bi, spp, stream, attr);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, extra_token_kernel, p, (const int32_t *)bi.seg_indptr,
+                                       (const int32_t *)bi.weight_indices, (const int32_t *)bi.permutation,
+                                       (const int32_t *)bi.num_segments_dev, (int32_t *)bi.status, spp);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

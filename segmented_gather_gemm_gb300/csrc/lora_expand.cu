@@ -1,4 +1,6 @@
 // Instantiations of the LoRA kernel, expand mode (token tile x buffer rank).
+// Expand-only calls on 128-token tiles with R >= 16 run on the streaming
+// tcgen05 expand (lora_stream.cu) instead.
 #include "lora_tma.cuh"
 
 namespace csgmv {
@@ -16,9 +18,6 @@ const void *lora_kernel_expand(int tm, int rmax, bool tc) {
     CSGMV_K(128, 32)
     CSGMV_K(128, 64)
 #undef CSGMV_K
-    if (tc && tm == 128 && rmax == 16) return reinterpret_cast<const void *>(lora_tma_kernel<128, 16, kModeExpand, true>);
-    if (tc && tm == 128 && rmax == 32) return reinterpret_cast<const void *>(lora_tma_kernel<128, 32, kModeExpand, true>);
-    if (tc && tm == 128 && rmax == 64) return reinterpret_cast<const void *>(lora_tma_kernel<128, 64, kModeExpand, true>);
     return nullptr;
 }
 

@@ -9,16 +9,15 @@
 
 #include "lora_small.cuh"
 #include "lora_stream.cuh"
-#include "lora_ws.cuh"
 
 namespace csgmv {
 
 const void *lora_kernel_fused(int tm, int rmax, bool tc);
 const void *lora_kernel_shrink(int tm, int rmax, bool tc);
 const void *lora_kernel_expand(int tm, int rmax, bool tc);
-const void *lora_kernel_ws(int mode, int rmax);
 const void *lora_kernel_small(int mode, int tm, int rmax);
 const void *lora_kernel_stream();
+const void *lora_kernel_sshrink();
 
 namespace {
 
@@ -43,6 +42,7 @@ cudaError_t encoder() {
 // `row_bytes` bytes, box of box_inner x box_outer elements.
 bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    if (!g_encode) return false;  // every launcher resolves it (encoder()) first
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_bytes};
     cuuint32_t box[2] = {box_inner, box_outer};
@@ -53,14 +53,31 @@ bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
     return r == CUDA_SUCCESS;
 }
 
-// One-row boxes of x for TMA 4-row gathers (128-token tiles whose tokens are
-// not consecutive); otherwise it points at a valid tensor.
-bool encode_row_gathers(TmaKernelParams &k, int mode, int s) {
+CUtensorMapSwizzle swizzle_for_row_bytes(int bytes) {
+    return bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+         : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+         : bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
+}
+
+// B of the expand: one (L, N, R) tensor in tmB (box R x box_rows), or, with
+// separate slice tensors, slice j in tmBs[j] (box R x 64); unused maps are
+// copies of a valid one.
+bool encode_b(TmaKernelParams &k, int L, uint32_t box_rows) {
     const LoraParams &p = k.p;
-    if (k.row_tma && mode != kModeExpand)
-        return encode_2d(&k.tmXg, p.x, (uint64_t)p.K, (uint64_t)s, (uint64_t)p.K * 2, 64, 1,
-                         CU_TENSOR_MAP_SWIZZLE_128B);
-    k.tmXg = k.tmA;
+    const CUtensorMapSwizzle sw = swizzle_for_row_bytes(p.R * 2);
+    if (!p.b_tuple) {
+        if (!encode_2d(&k.tmB, p.B, (uint64_t)p.R, (uint64_t)L * p.N, (uint64_t)p.R * 2, p.R, box_rows, sw))
+            return false;
+        for (int j = 0; j < kMaxSlices; ++j) k.tmBs[j] = k.tmB;
+        return true;
+    }
+    for (int j = 0; j < kMaxSlices; ++j) {
+        const int jj = j < p.c ? j : 0;
+        if (!encode_2d(&k.tmBs[j], p.Bs[jj], (uint64_t)p.R, (uint64_t)L * p.b_rows[jj], (uint64_t)p.R * 2, p.R, 64,
+                       sw))
+            return false;
+    }
+    k.tmB = k.tmBs[0];
     return true;
 }
 
@@ -180,47 +197,6 @@ size_t carve(TmaKernelParams &k, int mode, int tm, int cs, int S1, int S2, bool 
     return off + 1024;  // slack for aligning the dynamic window to 1024 bytes
 }
 
-CUtensorMapSwizzle swizzle_for_row_bytes(int bytes) {
-    return bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
-         : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-         : bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
-}
-
-// Shared-memory carve-up of the warp-specialized kernel.  The barriers, run
-// table and token lists come first; the rings and operand tiles start on
-// 1024-byte boundaries (128-byte swizzle).  No slack is reserved: the kernel
-// checks that its dynamic window starts on a 1024-byte boundary.
-size_t carve_ws(TmaKernelParams &k, int mode, int S1, int S2) {
-    const int R = k.p.R;
-    const int cR = k.p.c * R;
-    size_t off = 0;
-    auto take = [&](size_t bytes, size_t align) {
-        off = align_up(off, align);
-        size_t o = off;
-        off += bytes;
-        return (int)o;
-    };
-    k.S1 = mode == kModeExpand ? 1 : S1;
-    k.S2 = mode == kModeShrink ? 2 : S2;
-    k.o_bar = take((size_t)(2 * k.S1 + 3 * k.S2 + 12) * 8 + 16, 16);
-    k.o_run = take((size_t)(5 * k.runcap + 1 + 32) * 4, 16);
-    k.o_tok = take((size_t)(2 * 128 + 2) * 4, 16);
-    k.a_rows = (int)align_up((size_t)cR, 16);
-    k.o_sh = k.o_ah = k.o_ex = k.o_bring = 0;
-    k.sh_a = k.sh_stage = k.ex_b = k.ex_stage = 0;
-    if (mode != kModeExpand) {
-        k.sh_a = 128 * 128;
-        k.sh_stage = (int)align_up((size_t)k.sh_a + (size_t)k.a_rows * 128, 1024);
-        k.o_sh = take((size_t)k.S1 * k.sh_stage, 1024);
-    }
-    if (mode != kModeShrink) {
-        k.o_ah = take((size_t)k.p.c * 2 * kTcAhBytes, 1024);
-        k.o_ex = take((size_t)k.S2 * kWsBaseBytes, 1024);
-        k.o_bring = take((size_t)k.S2 * kWsCols * R * 2, 1024);
-    }
-    // at least 116 KB, so that one CTA holds an SM (and its 512 TMEM columns)
-    return std::max(off, (size_t)116 * 1024);
-}
 
 // Most slices that one CTA's column range spans, for nsplit * cs column
 // parts (the device split in column_range()).
@@ -357,8 +333,7 @@ cudaError_t launch_lora_small(int mode, LoraParams &p, const csgmv_batch_info &b
         ok = ok && encode_2d(&k.tmA, p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2, 64, k.a_rows,
                              CU_TENSOR_MAP_SWIZZLE_128B);
     if (mode != kModeShrink)
-        ok = ok && encode_2d(&k.tmB, p.B, (uint64_t)p.R, (uint64_t)L * p.N, (uint64_t)p.R * 2, p.R, 256,
-                             swizzle_for_row_bytes(p.R * 2));
+        ok = ok && encode_b(k, L, 256);
     if (mode == kModeExpand) k.tmA = k.tmB;
     if (mode == kModeShrink) k.tmB = k.tmA;
     k.tmX = k.tmY = k.tmXg = k.tmA;
@@ -390,82 +365,114 @@ cudaError_t launch_lora_small(int mode, LoraParams &p, const csgmv_batch_info &b
     return cudaGetLastError();
 }
 
-// 128-token tiles on the warp-specialized tcgen05 kernel (one CTA per SM).
-cudaError_t launch_lora_ws(int mode, LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream,
-                           LaunchInfo *info, int rmax) {
-    const void *fn = lora_kernel_ws(mode, rmax);
-    if (!fn) return cudaErrorInvalidValue;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+// Shared-memory carve-up of the streaming expand kernel for ring depth S;
+// returns the bytes needed (with slack for aligning the window to 1024).
+size_t carve_stream(StreamParams &k, int Sy) {
+    size_t off = 0;
+    auto take = [&](size_t bytes, size_t align) {
+        off = align_up(off, align);
+        size_t o = off;
+        off += bytes;
+        return (int)o;
+    };
+    k.Sy = Sy;
+    k.Sb = kStBSlots;
+    k.y_slot_bytes = kStBoxes * kStTileBytes;
+    k.b_slot_bytes = kStCols * k.p.R * 2;
+    k.o_bar = take((size_t)(2 * k.Sb + 2 * Sy + 2 * kStAcc + 4) * 8 + 16, 16);
+    k.o_run = take((size_t)(5 * k.runcap + 1 + 32) * 4, 16);
+    k.o_tok = take((size_t)(2 * 128 + 4) * 4, 16);
+    k.o_op = take((size_t)4 * kStTileBytes, 1024);
+    k.o_bring = take((size_t)k.Sb * k.b_slot_bytes, 1024);
+    k.o_yring = take((size_t)Sy * k.y_slot_bytes, 1024);
+    // at least 116 KB, so that one CTA holds an SM (and its 512 TMEM columns)
+    return std::max(off + 1024, (size_t)116 * 1024);
+}
+
+// Shared-memory carve-up of the streaming shrink kernel for ring depth S.
+size_t carve_sshrink(ShrinkParams &k, int S) {
+    size_t off = 0;
+    auto take = [&](size_t bytes, size_t align) {
+        off = align_up(off, align);
+        size_t o = off;
+        off += bytes;
+        return (int)o;
+    };
+    k.S = S;
+    k.stage_bytes = (int)align_up((size_t)128 * 128 + align_up((size_t)k.p.c * k.p.R, 16) * 128, 1024);
+    k.o_bar = take((size_t)(2 * S + 6) * 8 + 16, 16);
+    k.o_run = take((size_t)(5 * k.runcap + 1 + 32) * 4, 16);
+    k.o_tok = take((size_t)(2 * 128 + 2) * 4, 16);
+    k.o_ring = take((size_t)S * k.stage_bytes, 1024);
+    return std::max(off + 1024, (size_t)116 * 1024);
+}
+
+// Shrink on 128-token tiles: the streaming tcgen05 kernel, one CTA per SM.
+// K is cut into P <= max_parts parts (P > 1 only into an fp32 workspace of
+// max_parts planes of p.h_plane elements), chosen so that the units fill the
+// CTAs' last wave best; *parts_out gets P.
+cudaError_t launch_lora_sshrink(LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream, LaunchInfo *info,
+                                int max_parts, int *parts_out) {
+    const void *fn = lora_kernel_sshrink();
+    cudaError_t e = encoder();  // the tensor-map encoder, resolved on first use
     if (e != cudaSuccess) return e;
-    TmaKernelParams k;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    ShrinkParams k;
     memset(&k, 0, sizeof k);
     k.p = p;
     k.max_segments = bi.max_segments;
     k.runcap = std::max(1, std::min(bi.max_segments, bi.max_loras + std::max(bi.max_bs, 1)));
     const size_t budget = 227 * 1024;
-    // S2 even: expand stages go in pairs; a shrink-only launch has no expand
-    // ring, so its shrink ring takes the room
-    int S1 = mode == kModeShrink ? 8 : 4, S2 = 8;
-    size_t smem = carve_ws(k, mode, S1, S2);
-    while (smem > budget) {
-        if (mode == kModeShrink && S1 > 2) --S1;
-        else if (S2 > 4) S2 -= 2;
-        else if (S1 > 2) --S1;
-        else if (S2 > 2) S2 -= 2;
-        else return cudaErrorInvalidConfiguration;
-        smem = carve_ws(k, mode, S1, S2);
-    }
+    int S = 8;
+    size_t smem = carve_sshrink(k, S);
+    while (smem > budget && S > 2) smem = carve_sshrink(k, --S);
+    if (smem > budget) return cudaErrorInvalidConfiguration;
     e = ensure_attrs(fn, dev, 1);
     if (e != cudaSuccess) return e;
     int res = 0;
-    e = resident(fn, dev, 1, smem, &res, kWsThreads);
+    e = resident(fn, dev, 1, smem, &res, kShThreads);
     if (e != cudaSuccess) return e;
     if (res < 1) return cudaErrorInvalidConfiguration;
 
     const int s = p.num_tokens;
     const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
+    const int tiles_est = std::max(1, (s + 127) / 128 + slots / 2);
     const int tiles_ub = (s + 127) / 128 + std::min(std::max(bi.bs, 1), std::max(bi.max_loras, 1));
-    const int tiles_est = (s + 127) / 128 + slots / 2;
-    if (mode == kModeShrink) {
-        k.p.nsplit = 1;
-    } else {
-        // column blocks per tile: about two units per CTA, each block at
-        // least 512 columns wide
-        const int nblk = (p.off[p.c] - p.off[0] + 63) / 64;
-        const int want = (2 * res + tiles_est - 1) / std::max(tiles_est, 1);
-        k.p.nsplit = std::max(1, std::min(want, std::max(1, nblk / 8)));
+    const int nkc = (int)((p.K + 63) / 64);
+    // parts of K: the best-filled last wave of units, at least four K chunks a part
+    int best_P = 1;
+    double best_fill = 0.0;
+    for (int P = 1; P <= std::max(1, max_parts); ++P) {
+        const int kc = (nkc + P - 1) / P;
+        const int Pe = (nkc + kc - 1) / kc;
+        if (Pe != P || (P > 1 && kc < 4)) continue;
+        const int64_t units = (int64_t)tiles_est * P;
+        const int64_t waves = (units + res - 1) / res;
+        const double fill = (double)units / (double)(waves * res);
+        if (fill > best_fill + 0.02) { best_fill = fill; best_P = P; }
     }
-    const int64_t units_ub = (int64_t)tiles_ub * k.p.nsplit;
+    k.P = best_P;
+    k.kc_per = (nkc + best_P - 1) / best_P;
+    k.plane = p.h_plane;
+    if (parts_out) *parts_out = best_P;
+    const int64_t units_ub = (int64_t)tiles_ub * best_P;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(res, units_ub));
 
     const int L = bi.max_loras;
     const int cR = p.c * p.R;
-    bool ok = true;
-    if (mode != kModeShrink)
-        ok = ok && encode_2d(&k.tmB, p.B, (uint64_t)p.R, (uint64_t)L * p.N, (uint64_t)p.R * 2, p.R, kWsCols,
-                             swizzle_for_row_bytes(p.R * 2));
-    if (mode != kModeExpand) {
-        ok = ok && encode_2d(&k.tmA, p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2, 64, k.a_rows,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
-        ok = ok && encode_2d(&k.tmX, p.x, (uint64_t)p.K, (uint64_t)s, (uint64_t)p.K * 2, 64, 128,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
-    } else {
-        k.tmA = k.tmX = k.tmB;
-    }
-    if (mode != kModeShrink)  // base loads (when accumulating) and whole-tile stores
-        ok = ok && encode_2d(&k.tmY, p.y, (uint64_t)p.N, (uint64_t)s, (uint64_t)p.N * 2, 64, 128,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
-    else
-        k.tmY = k.tmA;
-    if (mode == kModeShrink) k.tmB = k.tmA;
-    k.row_tma = 1;
-    ok = ok && encode_row_gathers(k, mode, s);
+    bool ok = encode_2d(&k.tmX, p.x, (uint64_t)p.K, (uint64_t)s, (uint64_t)p.K * 2, 64, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && encode_2d(&k.tmXg, p.x, (uint64_t)p.K, (uint64_t)s, (uint64_t)p.K * 2, 64, 1,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && encode_2d(&k.tmA, p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2, 64, 16,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return cudaErrorInvalidValue;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(kWsThreads, 1, 1);
+    cfg.blockDim = dim3(kShThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -474,7 +481,7 @@ cudaError_t launch_lora_ws(int mode, LoraParams &p, const csgmv_batch_info &bi, 
     cfg.numAttrs = 1;
     if (info) {
         info->tm = 128;
-        info->crmax = rmax;
+        info->crmax = p.R;
         info->cluster = 1;
         info->grid = grid;
         info->smem = smem;
@@ -485,34 +492,15 @@ cudaError_t launch_lora_ws(int mode, LoraParams &p, const csgmv_batch_info &bi, 
     return cudaGetLastError();
 }
 
-// Shared-memory carve-up of the streaming expand kernel for ring depth S;
-// returns the bytes needed (with slack for aligning the window to 1024).
-size_t carve_stream(StreamParams &k, int S) {
-    size_t off = 0;
-    auto take = [&](size_t bytes, size_t align) {
-        off = align_up(off, align);
-        size_t o = off;
-        off += bytes;
-        return (int)o;
-    };
-    k.S = S;
-    k.slot_bytes = kStTileBytes + kStCols * k.p.R * 2;
-    k.o_bar = take((size_t)(4 * S + 2 * kStAcc + 4) * 8 + 16, 16);
-    k.o_run = take((size_t)(5 * k.runcap + 1 + 32) * 4, 16);
-    k.o_tok = take((size_t)(2 * 128 + 4) * 4, 16);
-    k.o_op = take((size_t)4 * kStTileBytes, 1024);
-    k.o_ring = take((size_t)S * k.slot_bytes, 1024);
-    // at least 116 KB, so that one CTA holds an SM (and its 512 TMEM columns)
-    return std::max(off + 1024, (size_t)116 * 1024);
-}
-
 // Expand-only calls on 128-token tiles: the streaming tcgen05 kernel, one CTA
 // per SM.  Units are (tile, column block inside one slice); the column block
 // is sized so that every CTA gets about sixteen units.
 cudaError_t launch_lora_stream(LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream, LaunchInfo *info) {
     const void *fn = lora_kernel_stream();
+    cudaError_t e = encoder();  // the tensor-map encoder, resolved on first use
+    if (e != cudaSuccess) return e;
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     StreamParams k;
     memset(&k, 0, sizeof k);
@@ -520,9 +508,11 @@ cudaError_t launch_lora_stream(LoraParams &p, const csgmv_batch_info &bi, cudaSt
     k.max_segments = bi.max_segments;
     k.runcap = std::max(1, std::min(bi.max_segments, bi.max_loras + std::max(bi.max_bs, 1)));
     const size_t budget = 227 * 1024;
-    int S = 8;
-    size_t smem = carve_stream(k, S);
-    while (smem > budget && S > 3) smem = carve_stream(k, --S);
+    // base slots: a multiple of the epilogue teams (each slot's barriers are
+    // then waited on by one team only), as many as fit
+    int Sy = 16 / kStBoxes / kStTeams * kStTeams;
+    size_t smem = carve_stream(k, Sy);
+    while (smem > budget && Sy > kStTeams) smem = carve_stream(k, Sy -= kStTeams);
     if (smem > budget) return cudaErrorInvalidConfiguration;
     e = ensure_attrs(fn, dev, 1);
     if (e != cudaSuccess) return e;
@@ -550,7 +540,7 @@ cudaError_t launch_lora_stream(LoraParams &p, const csgmv_batch_info &bi, cudaSt
     for (int j = 0; j < kMaxSlices; ++j) {
         const int jj = j < p.c ? j : 0;
         ok = ok && encode_2d(&k.tmB[j], p.Bs[jj], (uint64_t)p.R, (uint64_t)L * p.b_rows[jj], (uint64_t)p.R * 2, p.R,
-                             kStCols, swizzle_for_row_bytes(p.R * 2));
+                             64, swizzle_for_row_bytes(p.R * 2));  // one box per 64 columns of a stage
     }
     ok = ok && encode_2d(&k.tmY, p.y, (uint64_t)p.N, (uint64_t)s, (uint64_t)p.N * 2, 64, 128,
                          CU_TENSOR_MAP_SWIZZLE_128B);
@@ -597,12 +587,27 @@ bool qkv_split_pays(const LoraParams &p, const csgmv_batch_info &bi) {
     // CTA stream tens of thousands of columns; with h in the workspace, the
     // expand-only launch spreads column blocks of every tile over all SMs.
     if (tm <= 32) return p.off[p.c] - p.off[0] >= kWideCols;
-    // the shrink-only kernel for 128-token tiles and K <= 4096, then the
-    // tcgen05 expand: measured faster than the fused kernel on prefill
-    if (tm != 128 || p.K > 4096 || p.R < 16) return false;
-    for (int j = 0; j <= p.c; ++j)
-        if (p.off[j] % 16) return false;
-    return true;
+    // 128-token tiles: the streaming tcgen05 shrink and expand
+    return tm == 128 && p.R >= 16;
+}
+
+cudaError_t launch_qkv_split(LoraParams &ps, LoraParams &pe, const csgmv_batch_info &bi, cudaStream_t stream,
+                             size_t workspace_bytes) {
+    // parts of K the workspace holds (planes of s * c * R floats)
+    const size_t plane = (size_t)ps.num_tokens * ps.ldh;
+    int max_parts = (int)std::min<size_t>(kMaxKParts, plane ? workspace_bytes / (plane * 4) : 1);
+    cudaError_t e;
+    int parts = 1;
+    if (token_tile(ps, bi) == 128 && ps.R >= 16) {
+        ps.h_plane = (int64_t)plane;
+        e = launch_lora_sshrink(ps, bi, stream, nullptr, std::max(1, max_parts), &parts);
+    } else {
+        e = launch_lora(kModeShrink, ps, bi, stream, nullptr);
+    }
+    if (e != cudaSuccess) return e;
+    pe.h_parts = parts;
+    pe.h_plane = (int64_t)plane;
+    return launch_lora(kModeExpand, pe, bi, stream, nullptr);
 }
 
 cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream,
@@ -620,8 +625,9 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
     // Shrink-only calls on 128-token tiles of moderate K run on the
     // warp-specialized kernel (one CTA per tile, whole K, tcgen05); the fused
     // and expand calls measure faster on the cluster kernel.
-    if (tm == 128 && p.R >= 16 && mode == kModeShrink && p.K <= 4096)
-        return launch_lora_ws(mode, p, bi, stream, info, rmax);
+    // Shrink-only calls on 128-token tiles run on the streaming tcgen05
+    // shrink (h itself: one part of K).
+    if (tm == 128 && p.R >= 16 && mode == kModeShrink) return launch_lora_sshrink(p, bi, stream, info, 1, nullptr);
     // Expand-only calls on 128-token tiles stream base through the
     // warp-specialized tcgen05 expand.
     if (tm == 128 && p.R >= 16 && mode == kModeExpand) return launch_lora_stream(p, bi, stream, info);
@@ -726,8 +732,7 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
         ok = ok && encode_2d(&k.tmA, p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2, 64, k.a_rows,
                              CU_TENSOR_MAP_SWIZZLE_128B);
     if (mode != kModeShrink)
-        ok = ok && encode_2d(&k.tmB, p.B, (uint64_t)p.R, (uint64_t)L * p.N, (uint64_t)p.R * 2, p.R, nt,
-                             swizzle_for_row_bytes(p.R * 2));
+        ok = ok && encode_b(k, L, nt);
     if (mode == kModeExpand) k.tmA = k.tmB;
     if (mode == kModeShrink) k.tmB = k.tmA;
     // row boxes of x and base for 128-token tiles of consecutive tokens

@@ -181,7 +181,7 @@ __device__ void small_loop(const TmaKernelParams &k, unsigned char *smem, int q,
             mbar_arrive_expect_tx(&B.ex_full[e], bytes);
             if (b_copy)
                 for (int bb = 0; bb < G::NT / G::BBOX; ++bb)
-                    tma_load_2d(ys + k.ex_b + bb * G::BBOX * p.R * 2, &k.tmB, 0, U.w * (int)p.N + x0 + bb * G::BBOX,
+                    load_b_rows(k, ys + k.ex_b + bb * G::BBOX * p.R * 2, U.w, x0 + bb * G::BBOX, G::BBOX,
                                 &B.ex_full[e]);
             if (row_copy)
                 bulk_g2s(ys + my_row * k.ypitch, p.y + (int64_t)t * p.N + x0, (uint32_t)(x1 - x0) * 2, &B.ex_full[e]);
@@ -454,6 +454,8 @@ __global__ void __launch_bounds__(kConsumerThreads, 1) lora_small_kernel(const _
         fence_mbar_init();
         prefetch_tmap(&k.tmA);
         prefetch_tmap(&k.tmB);
+        if (k.p.b_tuple)
+            for (int j = 0; j < kMaxSlices; ++j) prefetch_tmap(&k.tmBs[j]);
     }
     int nruns = 0;
     const int ntiles = build_run_table<TM>(k, smem, &nruns);  // ends with __syncthreads

@@ -1,0 +1,267 @@
+// The streaming tcgen05 shrink kernel for 128-token tiles (see lora_stream.cuh).
+#include "lora_stream.cuh"
+
+namespace csgmv {
+
+namespace {
+
+struct ShBars {
+    uint64_t *full, *empty;           // [S]
+    uint64_t *acc_full, *acc_empty;   // [2]
+    uint64_t *tok_full, *tok_empty;   // [2]
+    uint32_t *tmem_slot;
+    int *tok;   // [2][128]
+    int *flag;  // [2] the tile's rows are consecutive tokens
+};
+
+__device__ __forceinline__ ShBars sh_bars(const ShrinkParams &k, unsigned char *smem) {
+    uint64_t *b = reinterpret_cast<uint64_t *>(smem + k.o_bar);
+    ShBars w;
+    w.full = b;
+    w.empty = b + k.S;
+    w.acc_full = b + 2 * k.S;
+    w.acc_empty = w.acc_full + 2;
+    w.tok_full = w.acc_empty + 2;
+    w.tok_empty = w.tok_full + 2;
+    w.tmem_slot = reinterpret_cast<uint32_t *>(w.tok_empty + 2);
+    w.tok = reinterpret_cast<int *>(smem + k.o_tok);
+    w.flag = w.tok + 256;
+    return w;
+}
+
+constexpr int kShAccCols = 256;  // TMEM columns per accumulator (c * R <= 192)
+
+// Unit u of the walk: part u / ntiles of K (so that the CTAs working at one
+// time share the A columns of one part) of token tile u % ntiles.  False when
+// the unit has no tensor-core work (rank 0, an invalid slot or rank).
+__device__ __forceinline__ bool sh_unit(const ShrinkParams &k, const int *tables, int nruns, int ntiles, int64_t u,
+                                        bool report, Unit &T, int &r, int &part, int &c0, int &c1) {
+    part = (int)(u / ntiles);
+    const int tile = (int)(u % ntiles);
+    T = tile_of<128>(tables, k.runcap, nruns, tile);
+    r = unit_rank(k.p, T, report && part == 0);
+    const int nkc = (int)((k.p.K + 63) / 64);
+    c0 = part * k.kc_per;
+    c1 = min(nkc, c0 + k.kc_per);
+    return r > 0 && c1 > c0;
+}
+
+// ------------------------------------------------------------------------------------- producer
+__device__ void sh_producer(const ShrinkParams &k, unsigned char *smem, const int *tables, int nruns, int ntiles,
+                            int64_t nunits) {
+    const LoraParams &p = k.p;
+    const int lane = threadIdx.x & 31;
+    const ShBars W = sh_bars(k, smem);
+    const int cR = p.c * p.R;
+    uint32_t it = 0, uc = 0;
+    for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
+        Unit T;
+        int r, part, c0, c1;
+        if (!sh_unit(k, tables, nruns, ntiles, u, lane == 0, T, r, part, c0, c1)) continue;
+        const int b = uc & 1;
+        mbar_wait(&W.tok_empty[b], ((uc >> 1) & 1) ^ 1, p.status, kStatusTimeout);
+        int *tok = W.tok + b * 128;
+        for (int m = lane; m < 128; m += 32) {
+            int t = -1;
+            if (m < T.M) {
+                t = p.permutation[T.p0 + m];
+                if (t < 0 || t >= p.num_tokens) {
+                    if (part == 0) atomicOr(p.status, CSGMV_STATUS_BAD_PERMUTATION);
+                    t = -1;
+                }
+            }
+            tok[m] = t;
+        }
+        __syncwarp();
+        const int t0 = tok[0];
+        bool mine = true;
+        for (int m = lane; m < T.M; m += 32) mine = mine && tok[m] == t0 + m;
+        const bool contig = __all_sync(0xffffffffu, mine) && t0 >= 0;
+        if (lane == 0) {
+            W.flag[b] = contig ? 1 : 0;
+            mbar_arrive(&W.tok_full[b]);
+        }
+        const int tfill = t0 >= 0 ? t0 : 0;
+        auto grow = [&](int mm) {
+            const int t = mm < T.M ? tok[mm] : -1;
+            return t >= 0 ? t : tfill;
+        };
+        const int n16 = (p.c * r + 15) / 16;  // 16-row boxes of A: rows [0, round16(c*r)) of the slot
+        const uint32_t bytes = 128 * 128 + (uint32_t)n16 * 16 * 128;
+        for (int ci = c0; ci < c1; ++ci, ++it) {
+            const int s = it % k.S;
+            mbar_wait(&W.empty[s], ((it / k.S) & 1) ^ 1, p.status, kStatusTimeout);
+            unsigned char *st = smem + k.o_ring + s * k.stage_bytes;
+            const int k0 = ci * 64;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&W.full[s], bytes);
+                for (int i = 0; i < n16; ++i)
+                    tma_load_2d(st + 128 * 128 + i * 16 * 128, &k.tmA, k0, T.w * cR + 16 * i, &W.full[s]);
+                if (contig) tma_load_2d(st, &k.tmX, k0, t0, &W.full[s]);
+            }
+            if (!contig) {
+                // lane l: tile rows 4l .. 4l+3 in one gather; rows past the tile
+                // (or of an invalid token) read a valid row that is never used
+                __syncwarp();  // after the byte count is posted
+                const int m = 4 * lane;
+                tma_gather4(st + m * 128, &k.tmXg, k0, grow(m), grow(m + 1), grow(m + 2), grow(m + 3), &W.full[s]);
+            }
+        }
+        ++uc;
+    }
+}
+
+// ------------------------------------------------------------------------------------- MMA issuer
+__device__ void sh_mma(const ShrinkParams &k, unsigned char *smem, const int *tables, int nruns, int ntiles,
+                       int64_t nunits, uint32_t tmem) {
+    const LoraParams &p = k.p;
+    const int lane = threadIdx.x & 31;
+    const ShBars W = sh_bars(k, smem);
+    uint32_t it = 0, uc = 0;
+    for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
+        Unit T;
+        int r, part, c0, c1;
+        if (!sh_unit(k, tables, nruns, ntiles, u, false, T, r, part, c0, c1)) continue;
+        const int b = uc & 1;
+        mbar_wait(&W.acc_empty[b], ((uc >> 1) & 1) ^ 1, p.status, kStatusTimeout);
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(128, (p.c * r + 15) & ~15);
+        const uint32_t d = tmem + (uint32_t)(b * kShAccCols);
+        for (int ci = c0; ci < c1; ++ci, ++it) {
+            const int s = it % k.S;
+            mbar_wait(&W.full[s], (it / k.S) & 1, p.status, kStatusTimeout);
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t xa = smem_u32(smem + k.o_ring + s * k.stage_bytes);
+                const uint32_t aa = xa + 128 * 128;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc_mma_bf16(d, smem_desc_kmajor(xa + ks * 32, 128), smem_desc_kmajor(aa + ks * 32, 128), idesc,
+                                ci > c0 || ks > 0);
+                tc_commit(&W.empty[s]);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) tc_commit(&W.acc_full[b]);
+        __syncwarp();
+        ++uc;
+    }
+    // the last stage releases land before the CTA (and its barriers) goes away
+    for (uint32_t g = it > (uint32_t)k.S ? it - k.S : 0; g < it; ++g)
+        mbar_wait(&W.empty[g % k.S], (g / k.S) & 1, p.status, kStatusTimeout);
+}
+
+// ------------------------------------------------------------------------------------- epilogue
+// h row of token t: part `part` of the workspace planes, or h itself.
+__device__ __forceinline__ void sh_store(const ShrinkParams &k, int part, int t, int col, float v) {
+    const LoraParams &p = k.p;
+    const int64_t o = (int64_t)part * k.plane + (int64_t)t * p.ldh + col;
+    if (p.h_f32) reinterpret_cast<float *>(p.h)[o] = v;
+    else reinterpret_cast<__nv_bfloat16 *>(p.h)[o] = __float2bfloat16_rn(v);
+}
+
+__device__ void sh_epilogue(const ShrinkParams &k, unsigned char *smem, const int *tables, int nruns, int ntiles,
+                            int64_t nunits, uint32_t tmem) {
+    const LoraParams &p = k.p;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;  // TMEM lanes (tile rows) 32q .. 32q+31
+    const int row = 32 * q + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    const ShBars W = sh_bars(k, smem);
+    const int cR = p.c * p.R;
+    uint32_t uc = 0;
+    for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
+        Unit T;
+        int r, part, c0, c1;
+        if (!sh_unit(k, tables, nruns, ntiles, u, false, T, r, part, c0, c1)) {
+            // h itself (one part): rows of rank-0 tokens are zero
+            if (r == 0 && k.P == 1 && row < T.M) {
+                const int t = p.permutation[T.p0 + row];
+                if (t >= 0 && t < p.num_tokens)
+                    for (int col = 0; col < cR; ++col) sh_store(k, 0, t, col, 0.f);
+            }
+            continue;
+        }
+        const int b = uc & 1;
+        mbar_wait(&W.tok_full[b], (uc >> 1) & 1, p.status, kStatusTimeout);
+        const int trow = row < T.M ? W.tok[b * 128 + row] : -1;
+        mbar_wait(&W.acc_full[b], (uc >> 1) & 1, p.status, kStatusTimeout);
+        tc_fence_after();
+        const int cr = p.c * r;
+        const int64_t o = (int64_t)part * k.plane + (int64_t)trow * p.ldh;
+        const bool vec = p.h_f32 && (o & 3) == 0;
+        for (int cc = 0; cc < cr; cc += 32) {
+            __syncwarp();  // tcgen05.ld is warp-wide
+            float v[32];
+            tmem_ld32(tmem + lane_base + (uint32_t)(b * kShAccCols + cc), v);
+            if (trow < 0) continue;
+            if (vec && cc + 32 <= cr) {
+                float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.h) + o + cc);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (cc + e < cr) sh_store(k, part, trow, cc + e, v[e]);
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&W.acc_empty[b]);
+        if (k.P == 1 && trow >= 0)  // h itself: columns [c*r, c*R) are zero
+            for (int col = cr; col < cR; ++col) sh_store(k, 0, trow, col, 0.f);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&W.tok_empty[b]);
+        ++uc;
+    }
+}
+
+__global__ void __launch_bounds__(kShThreads, 1) lora_stream_shrink_kernel(const __grid_constant__ ShrinkParams k) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const ShBars W = sh_bars(k, smem);
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < k.S; ++i) {
+            mbar_init(&W.full[i], 1);
+            mbar_init(&W.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&W.acc_full[i], 1);
+            mbar_init(&W.acc_empty[i], 4);
+            mbar_init(&W.tok_full[i], 1);
+            mbar_init(&W.tok_empty[i], 4);
+        }
+        fence_mbar_init();
+        prefetch_tmap(&k.tmX);
+        prefetch_tmap(&k.tmXg);
+        prefetch_tmap(&k.tmA);
+    }
+    if (warp == 1) {  // one warp owns the TMEM accumulators of the CTA
+        tmem_alloc(W.tmem_slot, 2 * kShAccCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    int nruns = 0;
+    int *tables = reinterpret_cast<int *>(smem + k.o_run);
+    const int ntiles = build_run_table_raw<128>(k.p, k.max_segments, k.runcap, tables, &nruns);  // ends with __syncthreads
+    tc_fence_after();
+    const uint32_t tmem = *W.tmem_slot;
+    const int64_t nunits = (int64_t)ntiles * k.P;
+    if (warp == 0) sh_producer(k, smem, tables, nruns, ntiles, nunits);
+    else if (warp == 1) sh_mma(k, smem, tables, nruns, ntiles, nunits, tmem);
+    else sh_epilogue(k, smem, tables, nruns, ntiles, nunits, tmem);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 2 * kShAccCols);
+    }
+}
+
+}  // namespace
+
+const void *lora_kernel_sshrink() { return reinterpret_cast<const void *>(lora_stream_shrink_kernel); }
+
+}  // namespace csgmv

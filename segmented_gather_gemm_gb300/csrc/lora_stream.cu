@@ -4,9 +4,10 @@
 namespace csgmv {
 
 struct StBars {
-    uint64_t *b_full, *b_empty, *y_full, *y_empty;  // [S]
-    uint64_t *acc_full, *acc_empty;                 // [kStAcc]
-    uint64_t *op_full, *op_empty;                   // [2]
+    uint64_t *b_full, *b_empty;      // [Sb]
+    uint64_t *y_full, *y_empty;      // [Sy]
+    uint64_t *acc_full, *acc_empty;  // [kStAcc]
+    uint64_t *op_full, *op_empty;    // [2]
     uint32_t *tmem_slot;
     int *tok;   // [2][128] token of each tile row (-1: none)
     int *flag;  // [2] the tile's rows are consecutive tokens; [2, 4) scratch
@@ -16,10 +17,10 @@ __device__ __forceinline__ StBars st_bars(const StreamParams &k, unsigned char *
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + k.o_bar);
     StBars w;
     w.b_full = b;
-    w.b_empty = b + k.S;
-    w.y_full = b + 2 * k.S;
-    w.y_empty = b + 3 * k.S;
-    w.acc_full = b + 4 * k.S;
+    w.b_empty = b + k.Sb;
+    w.y_full = b + 2 * k.Sb;
+    w.y_empty = w.y_full + k.Sy;
+    w.acc_full = w.y_empty + k.Sy;
     w.acc_empty = w.acc_full + kStAcc;
     w.op_full = w.acc_empty + kStAcc;
     w.op_empty = w.op_full + 2;
@@ -59,13 +60,44 @@ __device__ __forceinline__ bool st_unit(const StreamParams &k, const int *tables
     return r > 0 && U.nt > 0;
 }
 
-// ------------------------------------------------------------------------------------- producer
+// ------------------------------------------------------------------------------------- producers
+// B tiles: they need no token list, so this warp runs ahead of the operand
+// tiles by as many stages as the B ring holds.
+__device__ void st_b_producer(const StreamParams &k, unsigned char *smem, const int *tables, int nruns,
+                              int64_t nunits) {
+    const LoraParams &p = k.p;
+    const int lane = threadIdx.x & 31;
+    const StBars W = st_bars(k, smem);
+    const uint32_t Bbytes = (uint32_t)kStCols * p.R * 2;  // kStBoxes boxes of 64 B rows
+    uint32_t g = 0;
+    for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
+        StUnit U;
+        int r;
+        if (!st_unit(k, tables, nruns, u, false, U, r)) continue;
+        // row in the 2-D view of B_j of column x of the unit's slice
+        const int brow = U.w * p.b_rows[U.j] + p.b_row0[U.j] - p.off[U.j];
+        for (int i = 0; i < U.nt; ++i, ++g) {
+            const int sb = g % k.Sb;
+            const int x0 = U.n0 + i * kStCols;
+            mbar_wait(&W.b_empty[sb], ((g / k.Sb) & 1) ^ 1, p.status, kStatusTimeout);
+            if (lane == 0) {
+                unsigned char *bs = smem + k.o_bring + sb * k.b_slot_bytes;
+                mbar_arrive_expect_tx(&W.b_full[sb], Bbytes);
+#pragma unroll
+                for (int bx = 0; bx < kStBoxes; ++bx)
+                    tma_load_2d(bs + bx * 64 * p.R * 2, &k.tmB[U.j], 0, brow + x0 + 64 * bx, &W.b_full[sb]);
+            }
+            __syncwarp();
+        }
+    }
+}
+
+// Base rows of every stage, through the tile's token list.
 __device__ void st_producer(const StreamParams &k, unsigned char *smem, const int *tables, int nruns,
                             int64_t nunits) {
     const LoraParams &p = k.p;
     const int lane = threadIdx.x & 31;
     const StBars W = st_bars(k, smem);
-    const uint32_t Bbytes = (uint32_t)kStCols * p.R * 2;
     uint32_t g = 0, uc = 0;
     for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
         StUnit U;
@@ -77,33 +109,34 @@ __device__ void st_producer(const StreamParams &k, unsigned char *smem, const in
         const bool contig = W.flag[b] != 0;
         const int t0 = tok[0];
         const int tfill = t0 >= 0 ? t0 : 0;
-        // row in the 2-D view of B_j of column x of the unit's slice
-        const int brow = U.w * p.b_rows[U.j] + p.b_row0[U.j] - p.off[U.j];
         for (int i = 0; i < U.nt; ++i, ++g) {
-            const int s = g % k.S;
-            const uint32_t ph = (g / k.S) & 1;
-            mbar_wait(&W.y_empty[s], ph ^ 1, p.status, kStatusTimeout);
-            mbar_wait(&W.b_empty[s], ph ^ 1, p.status, kStatusTimeout);
-            unsigned char *slot = smem + k.o_ring + s * k.slot_bytes;
+            const int sy = g % k.Sy;
             const int x0 = U.n0 + i * kStCols;
+            mbar_wait(&W.y_empty[sy], ((g / k.Sy) & 1) ^ 1, p.status, kStatusTimeout);
+            unsigned char *ys = smem + k.o_yring + sy * k.y_slot_bytes;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&W.b_full[s], Bbytes);
-                tma_load_2d(slot + kStTileBytes, &k.tmB[U.j], 0, brow + x0, &W.b_full[s]);
-                mbar_arrive_expect_tx(&W.y_full[s], p.accumulate ? kStTileBytes : 0);
-                if (p.accumulate && contig) tma_load_2d(slot, &k.tmY, x0, t0, &W.y_full[s]);
+                mbar_arrive_expect_tx(&W.y_full[sy], p.accumulate ? kStBoxes * kStTileBytes : 0);
+                if (p.accumulate && contig)
+#pragma unroll
+                    for (int bx = 0; bx < kStBoxes; ++bx)
+                        tma_load_2d(ys + bx * kStTileBytes, &k.tmY, x0 + 64 * bx, t0, &W.y_full[sy]);
             }
             if (p.accumulate && !contig) {
-                // lane l: tile rows 4l .. 4l+3 in one gather; rows past the tile
-                // (or of an invalid token) read a valid row that is never used
+                // lane l: tile rows 4l .. 4l+3 in one gather per box; rows past the
+                // tile (or of an invalid token) read a valid row that is never used
                 __syncwarp();  // after the byte count is posted
                 const int m = 4 * lane;
                 auto grow = [&](int mm) {
                     const int t = mm < U.M ? tok[mm] : -1;
                     return t >= 0 ? t : tfill;
                 };
-                tma_gather4(slot + m * 128, &k.tmYg, x0, grow(m), grow(m + 1), grow(m + 2), grow(m + 3),
-                            &W.y_full[s]);
+                const int r0 = grow(m), r1 = grow(m + 1), r2 = grow(m + 2), r3 = grow(m + 3);
+#pragma unroll
+                for (int bx = 0; bx < kStBoxes; ++bx)
+                    tma_gather4(ys + bx * kStTileBytes + m * 128, &k.tmYg, x0 + 64 * bx, r0, r1, r2, r3,
+                                &W.y_full[sy]);
             }
+            __syncwarp();
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&W.op_empty[b]);  // done with the token list
@@ -132,10 +165,10 @@ __device__ void st_mma(const StreamParams &k, unsigned char *smem, const int *ta
         const int ksteps = RK / 16;
         const uint32_t ahi = op0 + (uint32_t)(2 * b) * kStTileBytes, alo = ahi + kStTileBytes;
         for (int i = 0; i < U.nt; ++i, ++g) {
-            const int s = g % k.S;
+            const int sb = g % k.Sb;
             const int a = g % kStAcc;
-            mbar_wait(&W.b_full[s], (g / k.S) & 1, p.status, kStatusTimeout);
-            unsigned char *bs = smem + k.o_ring + s * k.slot_bytes + kStTileBytes;
+            mbar_wait(&W.b_full[sb], (g / k.Sb) & 1, p.status, kStatusTimeout);
+            unsigned char *bs = smem + k.o_bring + sb * k.b_slot_bytes;
             if (RK != r) {  // B columns [r, RK) are adapter padding (even NaN): zero them
                 const int c0 = r >> 3, nc = (RK >> 3) - c0;
                 for (int idx = lane; idx < kStCols * nc; idx += 32) {
@@ -161,7 +194,7 @@ __device__ void st_mma(const StreamParams &k, unsigned char *smem, const int *ta
                     tc_mma_bf16(d, smem_desc_kmajor(ahi + ks * 32, 128), bd, idesc, ks > 0);
                     tc_mma_bf16(d, smem_desc_kmajor(alo + ks * 32, 128), bd, idesc, true);
                 }
-                tc_commit(&W.b_empty[s]);
+                tc_commit(&W.b_empty[sb]);
                 tc_commit(&W.acc_full[a]);
             }
             __syncwarp();
@@ -169,23 +202,28 @@ __device__ void st_mma(const StreamParams &k, unsigned char *smem, const int *ta
         ++uc;
     }
     // the last slot releases land before the CTA (and its barriers) goes away
-    for (uint32_t gg = g > (uint32_t)k.S ? g - k.S : 0; gg < g; ++gg)
-        mbar_wait(&W.b_empty[gg % k.S], (gg / k.S) & 1, p.status, kStatusTimeout);
+    for (uint32_t gg = g > (uint32_t)k.Sb ? g - k.Sb : 0; gg < g; ++gg)
+        mbar_wait(&W.b_empty[gg % k.Sb], (gg / k.Sb) & 1, p.status, kStatusTimeout);
 }
 
 // ------------------------------------------------------------------------------------- operands
 // h[t][col .. col+7] as fp32 (0 past `r` columns of the slice, i.e. col >= lim).
+// fp32 h held as partial sums over parts of K is summed part by part, in order.
 __device__ __forceinline__ void st_h8(const LoraParams &p, int t, int col, int lim, float (&v)[8]) {
     const int64_t o = (int64_t)t * p.ldh + col;
     if (p.h_f32) {
-        const float *h = reinterpret_cast<const float *>(p.h) + o;
-        if (col + 8 <= lim && (o & 3) == 0) {
-            const float4 a = *reinterpret_cast<const float4 *>(h), b = *reinterpret_cast<const float4 *>(h + 4);
-            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-        } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = col + e < lim ? h[e] : 0.f;
+        for (int e = 0; e < 8; ++e) v[e] = 0.f;
+        for (int part = 0; part < p.h_parts; ++part) {
+            const float *h = reinterpret_cast<const float *>(p.h) + part * p.h_plane + o;
+            if (col + 8 <= lim && ((o + part * p.h_plane) & 3) == 0) {
+                const float4 a = *reinterpret_cast<const float4 *>(h), b = *reinterpret_cast<const float4 *>(h + 4);
+                v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+                v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] += col + e < lim ? h[e] : 0.f;
+            }
         }
     } else {
         const __nv_bfloat16 *h = reinterpret_cast<const __nv_bfloat16 *>(p.h) + o;
@@ -206,20 +244,20 @@ __device__ __forceinline__ void st_h8(const LoraParams &p, int t, int col, int l
 __device__ void st_operands(const StreamParams &k, unsigned char *smem, const int *tables, int nruns,
                             int64_t nunits) {
     const LoraParams &p = k.p;
-    const int otid = threadIdx.x - 64, lane = otid & 31, ow = otid >> 5;
+    const int lane = threadIdx.x & 31;
     const StBars W = st_bars(k, smem);
     uint32_t uc = 0;
     for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
         StUnit U;
         int r;
-        if (!st_unit(k, tables, nruns, u, otid == 0, U, r)) continue;
+        if (!st_unit(k, tables, nruns, u, lane == 0, U, r)) continue;
         const int b = uc & 1;
         mbar_wait(&W.op_empty[b], ((uc >> 1) & 1) ^ 1, p.status, kStatusTimeout);
         int *tok = W.tok + b * 128;
-        int tm[2];
+        int tm[4];
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const int m = otid + 64 * h2;
+        for (int h4 = 0; h4 < 4; ++h4) {  // tile rows lane, lane + 32, ...
+            const int m = lane + 32 * h4;
             int t = -1;
             if (m < U.M) {
                 t = p.permutation[U.p0 + m];
@@ -229,20 +267,18 @@ __device__ void st_operands(const StreamParams &k, unsigned char *smem, const in
                 }
             }
             tok[m] = t;
-            tm[h2] = t;
+            tm[h4] = t;
         }
-        named_bar_sync(kStOpBar, 64);
+        __syncwarp();
         const int t0 = tok[0];
         bool mine = true;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const int m = otid + 64 * h2;
-            if (m < U.M) mine = mine && tm[h2] == t0 + m;
+        for (int h4 = 0; h4 < 4; ++h4) {
+            const int m = lane + 32 * h4;
+            if (m < U.M) mine = mine && tm[h4] == t0 + m;
         }
-        const bool wall = __all_sync(0xffffffffu, mine);
-        if (lane == 0) W.flag[2 + ow] = wall ? 1 : 0;
-        named_bar_sync(kStOpBar, 64);
-        if (otid == 0) W.flag[b] = (W.flag[2] && W.flag[3] && t0 >= 0) ? 1 : 0;
+        const bool contig = __all_sync(0xffffffffu, mine) && t0 >= 0;
+        if (lane == 0) W.flag[b] = contig ? 1 : 0;
 
         // operand tiles: row m = token m of the tile, columns [0, RK) of slice j
         unsigned char *ahi = smem + k.o_op + (2 * b) * kStTileBytes;
@@ -250,9 +286,9 @@ __device__ void st_operands(const StreamParams &k, unsigned char *smem, const in
         const int RK = (r + 15) & ~15;
         const int col0 = U.j * r;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const int m = otid + 64 * h2;
-            const int t = tm[h2];
+        for (int h4 = 0; h4 < 4; ++h4) {
+            const int m = lane + 32 * h4;
+            const int t = tm[h4];
             for (int ch = 0; ch < RK / 8; ++ch) {
                 float v[8];
                 if (t >= 0) {
@@ -272,8 +308,8 @@ __device__ void st_operands(const StreamParams &k, unsigned char *smem, const in
             }
         }
         fence_proxy_async_smem();  // the operand tiles are read by the tensor core
-        named_bar_sync(kStOpBar, 64);
-        if (otid == 0) mbar_arrive(&W.op_full[b]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&W.op_full[b]);
         ++uc;
     }
 }
@@ -289,7 +325,6 @@ __device__ void st_epilogue(const StreamParams &k, unsigned char *smem, const in
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const StBars W = st_bars(k, smem);
     uint32_t g = 0, uc = 0;
-    int pending = -1;  // lane 0: the slot of this warp's last box store, not yet handed back
     for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
         StUnit U;
         int r;
@@ -311,63 +346,56 @@ __device__ void st_epilogue(const StreamParams &k, unsigned char *smem, const in
         const int trow = row < U.M ? tok[row] : -1;
         const float sigma = p.scalings[U.w];
         for (int i = 0; i < U.nt; ++i, ++g) {
-            if ((int)(g & 1) != team) continue;
-            const int s = g % k.S;
+            if ((int)(g % kStTeams) != team) continue;
+            const int sy = g % k.Sy;
             const int a = g % kStAcc;
             mbar_wait(&W.acc_full[a], (g / kStAcc) & 1, p.status, kStatusTimeout);
-            mbar_wait(&W.y_full[s], (g / k.S) & 1, p.status, kStatusTimeout);
+            mbar_wait(&W.y_full[sy], (g / k.Sy) & 1, p.status, kStatusTimeout);
             tc_fence_after();
-            __syncwarp();  // tcgen05.ld is warp-wide
-            float v[2][32];
-            tmem_ld32(tmem + lane_base + (uint32_t)(a * kStCols), v[0]);
-            tmem_ld32(tmem + lane_base + (uint32_t)(a * kStCols + 32), v[1]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&W.acc_empty[a]);
             const int x0 = U.n0 + i * kStCols;
             const int ncols = min(U.n1, x0 + kStCols) - x0;
             const bool full = box && ncols == kStCols;
-            unsigned char *ys = smem + k.o_ring + s * k.slot_bytes;
-            if (row < U.M && (full || trow >= 0)) {
+            unsigned char *ys = smem + k.o_yring + sy * k.y_slot_bytes;
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    if (8 * c8 < ncols) {
-                        uint4 *ptr = reinterpret_cast<uint4 *>(ys + row * 128 + ((c8 ^ (row & 7)) << 4));
-                        const float *vv = &v[c8 >> 2][8 * (c8 & 3)];
-                        uint4 bv = p.accumulate ? *ptr : make_uint4(0, 0, 0, 0);
-                        float2 f;
-                        f = unpack_bf16x2(bv.x); bv.x = pack_bf16x2(f.x + sigma * vv[0], f.y + sigma * vv[1]);
-                        f = unpack_bf16x2(bv.y); bv.y = pack_bf16x2(f.x + sigma * vv[2], f.y + sigma * vv[3]);
-                        f = unpack_bf16x2(bv.z); bv.z = pack_bf16x2(f.x + sigma * vv[4], f.y + sigma * vv[5]);
-                        f = unpack_bf16x2(bv.w); bv.w = pack_bf16x2(f.x + sigma * vv[6], f.y + sigma * vv[7]);
-                        if (full) *ptr = bv;
-                        else *reinterpret_cast<uint4 *>(p.y + (int64_t)trow * p.N + x0 + 8 * c8) = bv;
+            for (int bx = 0; bx < kStBoxes; ++bx) {
+                __syncwarp();  // tcgen05.ld is warp-wide
+                float v[64];
+                tmem_ld64(tmem + lane_base + (uint32_t)(a * kStCols + 64 * bx), v);
+                if (bx == kStBoxes - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&W.acc_empty[a]);
+                }
+                unsigned char *yb = ys + bx * kStTileBytes;
+                if (row < U.M && (full || trow >= 0)) {
+#pragma unroll
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        if (64 * bx + 8 * c8 < ncols) {
+                            uint4 *ptr = reinterpret_cast<uint4 *>(yb + row * 128 + ((c8 ^ (row & 7)) << 4));
+                            const float *vv = &v[8 * c8];
+                            uint4 bv = p.accumulate ? *ptr : make_uint4(0, 0, 0, 0);
+                            float2 f;
+                            f = unpack_bf16x2(bv.x); bv.x = pack_bf16x2(f.x + sigma * vv[0], f.y + sigma * vv[1]);
+                            f = unpack_bf16x2(bv.y); bv.y = pack_bf16x2(f.x + sigma * vv[2], f.y + sigma * vv[3]);
+                            f = unpack_bf16x2(bv.z); bv.z = pack_bf16x2(f.x + sigma * vv[4], f.y + sigma * vv[5]);
+                            f = unpack_bf16x2(bv.w); bv.w = pack_bf16x2(f.x + sigma * vv[6], f.y + sigma * vv[7]);
+                            if (full) *ptr = bv;
+                            else *reinterpret_cast<uint4 *>(p.y + (int64_t)trow * p.N + x0 + 64 * bx + 8 * c8) = bv;
+                        }
                     }
                 }
             }
-            if (full) {
-                fence_proxy_async_smem();  // the in-place rows before the TMA store reads them
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&k.tmYs, x0, t0 + 32 * q, ys + 32 * q * 128);
+            fence_proxy_async_smem();  // in-place rows before the TMA store reads them; reads before a refill
+            __syncwarp();
+            if (lane == 0) {
+                if (full) {  // the slot goes back once the stores have read this warp's rows
+#pragma unroll
+                    for (int bx = 0; bx < kStBoxes; ++bx)
+                        tma_store_2d(&k.tmYs, x0 + 64 * bx, t0 + 32 * q, ys + bx * kStTileBytes + 32 * q * 128);
                     bulk_commit();
-                    if (pending >= 0) {  // the previous store has read its rows: hand its slot back
-                        bulk_wait_read<1>();
-                        mbar_arrive(&W.y_empty[pending]);
-                    }
-                    pending = s;
+                    bulk_wait_read<0>();
                 }
-            } else {
-                fence_proxy_async_smem();  // this warp's reads of the slot before a TMA refills it
-                __syncwarp();
-                if (lane == 0) {
-                    if (pending >= 0) {
-                        bulk_wait_read<0>();
-                        mbar_arrive(&W.y_empty[pending]);
-                        pending = -1;
-                    }
-                    mbar_arrive(&W.y_empty[s]);
-                }
+                mbar_arrive(&W.y_empty[sy]);
             }
         }
         __syncwarp();
@@ -387,9 +415,11 @@ __global__ void __launch_bounds__(kStThreads, 1) lora_stream_expand_kernel(const
     const StBars W = st_bars(k, smem);
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < k.S; ++i) {
+        for (int i = 0; i < k.Sb; ++i) {
             mbar_init(&W.b_full[i], 1);
             mbar_init(&W.b_empty[i], 1);
+        }
+        for (int i = 0; i < k.Sy; ++i) {
             mbar_init(&W.y_full[i], 1);
             mbar_init(&W.y_empty[i], 4);  // the four warps of the team that takes the stage
         }
@@ -399,7 +429,7 @@ __global__ void __launch_bounds__(kStThreads, 1) lora_stream_expand_kernel(const
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&W.op_full[i], 1);
-            mbar_init(&W.op_empty[i], 1 + 8);  // producer + epilogue warps
+            mbar_init(&W.op_empty[i], 1 + kStEpiWarps);  // producer + epilogue warps
         }
         fence_mbar_init();
         for (int j = 0; j < kMaxSlices; ++j) prefetch_tmap(&k.tmB[j]);
@@ -408,7 +438,7 @@ __global__ void __launch_bounds__(kStThreads, 1) lora_stream_expand_kernel(const
         prefetch_tmap(&k.tmYg);
     }
     if (warp == 1) {  // one warp owns the TMEM accumulators of the CTA
-        tmem_alloc(W.tmem_slot, kStAcc * kStCols);
+        tmem_alloc(W.tmem_slot, kStTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -420,13 +450,14 @@ __global__ void __launch_bounds__(kStThreads, 1) lora_stream_expand_kernel(const
     const int64_t nunits = (int64_t)ntiles * k.upt;
     if (warp == 0) st_producer(k, smem, tables, nruns, nunits);
     else if (warp == 1) st_mma(k, smem, tables, nruns, nunits, tmem);
-    else if (warp < kStEpiWarp0) st_operands(k, smem, tables, nruns, nunits);
+    else if (warp == 2) st_operands(k, smem, tables, nruns, nunits);
+    else if (warp == 3) st_b_producer(k, smem, tables, nruns, nunits);
     else st_epilogue(k, smem, tables, nruns, nunits, tmem);
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kStAcc * kStCols);
+        tmem_dealloc(tmem, kStTmemCols);
     }
 }
 

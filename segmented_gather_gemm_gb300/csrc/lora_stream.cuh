@@ -11,23 +11,24 @@
 // fixed stride; every role runs the same unit walk and the roles are linked
 // only by mbarriers, so loads of later stages and units stream while earlier
 // ones are multiplied and written back:
-//   warp 0      producer: per 64-column stage, the slot's B rows (one TMA
-//               box) and the tile's base rows (one 128-row TMA box when the
-//               tile's tokens are consecutive, else 32 TMA 4-row gathers)
-//               into a ring of S slots;
+//   warp 0      base producer: per stage of kStCols columns, the tile's base
+//               rows (128-row TMA boxes when the tile's tokens are
+//               consecutive, else TMA 4-row gathers) into a ring of base
+//               slots;
+//   warp 3      B producer: per stage, the slot's B rows (one TMA box per 64
+//               columns) into a ring of B slots, running ahead of the rest;
 //   warp 1      MMA issuer: per stage, y_delta = h B^T on the tensor cores
 //               (h as a bf16 hi + lo pair, so it keeps ~16 bits) into one of
-//               eight TMEM accumulators; completions free the B part of a
-//               ring slot;
-//   warps 2, 3  operands: per unit, the token list and h of the unit's slice
+//               kStAcc TMEM accumulators; completions free the B slot;
+//   warp 2      operands: per unit, the token list and h of the unit's slice
 //               from global memory as bf16 hi / lo operand tiles (128-byte
 //               swizzle), double-buffered one unit ahead;
-//   warps 4-11  epilogue, two teams of four that take alternate stages: each
+//   warps 4..   epilogue, teams of four warps that take the stages in turn: each
 //               warp reads its 32 accumulator rows (tcgen05.ld), adds base in
 //               fp32 and writes the rounded rows back in place, then stores
-//               its 32 x 64 piece with one TMA box store (a full tile of
+//               its 32-row piece with TMA box stores (a full tile of
 //               consecutive tokens) or 16-byte row stores through the token
-//               list; a slot is handed back once its stores have read it.
+//               list; a base slot is handed back once its stores have read it.
 // Every wait is bounded; on a timeout the kernel sets a status bit and ends.
 #pragma once
 
@@ -35,13 +36,23 @@
 
 namespace csgmv {
 
-constexpr int kStWarps = 12;
+constexpr int kStTeams = 3;              // epilogue teams of four warps, taking stages in turn
+constexpr int kStEpiWarps = 4 * kStTeams;
+constexpr int kStWarps = 4 + kStEpiWarps;
 constexpr int kStThreads = kStWarps * 32;
-constexpr int kStCols = 64;              // output columns per stage
-constexpr int kStAcc = 8;                // TMEM accumulators of kStCols columns (all 512 columns)
-constexpr int kStTileBytes = 128 * 128;  // 128 rows x 64 bf16: a base stage or an operand tile
-constexpr int kStOpBar = 3;              // named barrier of the operand warps
+constexpr int kStBoxes = 1;              // 64-column boxes per stage
+constexpr int kStCols = 64 * kStBoxes;   // output columns per stage
+// TMEM accumulators of kStCols columns.  Every mbarrier of the epilogue is
+// waited on by one team only: stage g takes accumulator g % kStAcc, base slot
+// g % Sy and team g % kStTeams, so kStAcc and Sy are multiples of kStTeams (a
+// team that waited on a barrier another team also waits on could take a
+// phase two completions old for the current one).
+constexpr int kStTmemCols = 512;         // the allocation: a power of two
+constexpr int kStAcc = (kStTmemCols / kStCols) / kStTeams * kStTeams;
+constexpr int kStTileBytes = 128 * 128;  // 128 rows x 64 bf16: one base box or an operand tile
+constexpr int kStBSlots = 4;             // B tiles in flight (needed only until their MMAs are done)
 constexpr int kStEpiWarp0 = 4;
+static_assert(kStAcc >= kStTeams, "every team needs an accumulator");
 
 struct StreamParams {
     CUtensorMap tmB[kMaxSlices];  // slice j of B: L * b_rows[j] rows of R bf16, box R x 64
@@ -52,9 +63,43 @@ struct StreamParams {
     int runcap, max_segments;
     int cb;                       // columns of a unit (multiple of 64)
     int upt;                      // units per tile: sum over slices of ceil(width / cb)
-    int S;                        // ring slots
-    int o_bar, o_run, o_tok, o_op, o_ring;
-    int slot_bytes;               // base tile + B tile
+    int Sy, Sb;                   // base slots, B slots
+    int o_bar, o_run, o_tok, o_op, o_yring, o_bring;
+    int y_slot_bytes, b_slot_bytes;  // kStBoxes base boxes; kStCols rows of B
+};
+
+// Streaming tcgen05 shrink for 128-token tiles (run_lora_a_sgemm):
+//     h[t][j*r + k] = sum_i x[t][i] * A[w][j*r + k][i]
+// One CTA per SM walks its units (a tile of up to 128 tokens of one slot x
+// one of P parts of K) with a fixed stride:
+//   warp 0      producer: the tile's token list, then per 64-wide K chunk the
+//               x rows (one 128-row TMA box for consecutive tokens, else 32
+//               TMA 4-row gathers) and the slot's A rows [0, round16(c*r)) as
+//               16-row boxes, into a ring of S stages;
+//   warp 1      MMA issuer: h_part = x A^T over the unit's K chunks into one of
+//               two TMEM accumulators (the next unit's MMAs run while the last
+//               one is written out);
+//   warps 2-5   epilogue: each warp its 32 rows of the accumulator
+//               (tcgen05.ld), written as fp32 (or bf16) h rows.
+// With P > 1 (the csgmv_qkv workspace path) part p of K goes to plane p of
+// the workspace and the expand sums the planes in order; P = 1 writes h
+// itself, with zeros in columns [c*r, c*R) and in rows of rank-0 tokens.
+constexpr int kShWarps = 6;
+constexpr int kShThreads = kShWarps * 32;
+constexpr int kShEpiWarp0 = 2;
+
+struct ShrinkParams {
+    CUtensorMap tmX;   // x (s rows, K): box 64 x 128, 128-byte swizzle
+    CUtensorMap tmXg;  // the same, box 64 x 1 (4-row gathers)
+    CUtensorMap tmA;   // A (L * c * R rows, K): box 64 x 16, 128-byte swizzle
+    LoraParams p;
+    int runcap, max_segments;
+    int P;             // parts of K
+    int kc_per;        // 64-wide K chunks per part
+    int S;             // ring stages
+    int o_bar, o_run, o_tok, o_ring;
+    int stage_bytes;   // x tile + A tile of round16(c * R) rows
+    int64_t plane;     // elements of h between two parts (P > 1)
 };
 
 }  // namespace csgmv

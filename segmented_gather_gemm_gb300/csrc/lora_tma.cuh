@@ -53,7 +53,8 @@ struct TmaKernelParams {
     CUtensorMap tmB;    // B (L*N rows, R):   box R x NT, swizzle of the R*2-byte row
     CUtensorMap tmX;    // x (s rows, K): box 64 x TM, 128B swizzle (128-token tiles)
     CUtensorMap tmY;    // base / y (s rows, N): box 64 x TM, 128B swizzle (128-token tiles)
-    CUtensorMap tmXg;   // warp-specialized shrink: x, box 64 x 1, 128B swizzle, for 4-row gathers
+    CUtensorMap tmXg;   // x, box 64 x 1, 128B swizzle, for 4-row gathers
+    CUtensorMap tmBs[kMaxSlices];  // B as separate slice tensors (p.b_tuple): box R x 64 of slice j
     int row_tma;        // 1: tmX / tmY are valid; tiles of consecutive tokens load rows by TMA
     LoraParams p;
     int S1, S2;        // shrink / expand ring depth
@@ -270,6 +271,26 @@ __device__ __forceinline__ int slice_at(const LoraParams &p, int col) {
     int j = 0;
     while (j + 1 < p.c && col >= p.off[j + 1]) ++j;
     return j;
+}
+
+// B rows of output columns [x0, x0 + rows) of slot w into dst (rows * R bf16,
+// the layout of one box of tmB), completing on bar.  One tensor: one box of
+// tmB.  Separate slice tensors: 64-row boxes, each from the slice its first
+// column falls in (slice offsets and x0 are multiples of 64, so no box
+// crosses a slice; columns past the last slice read rows that are not used).
+__device__ __forceinline__ void load_b_rows(const TmaKernelParams &k, void *dst, int w, int x0, int rows,
+                                            uint64_t *bar) {
+    const LoraParams &p = k.p;
+    if (!p.b_tuple) {
+        tma_load_2d(dst, &k.tmB, 0, w * (int)p.N + x0, bar);
+        return;
+    }
+    for (int r0 = 0; r0 < rows; r0 += 64) {
+        const int col = x0 + r0;
+        const int j = slice_at(p, col);
+        tma_load_2d(static_cast<unsigned char *>(dst) + r0 * p.R * 2, &k.tmBs[j], 0,
+                    w * p.b_rows[j] + p.b_row0[j] + (col - p.off[j]), bar);
+    }
 }
 
 // Whether unit U is worked on at all; rank-0 slots have no work, invalid
@@ -597,7 +618,7 @@ __device__ void consumer_loop(const TmaKernelParams &k, unsigned char *smem, int
             const bool base_tma = rows_tma && p.accumulate;
             if (tid == 0) {  // the B rows of this column tile: one TMA box (base rows: NB64 more)
                 mbar_arrive_expect_tx(&B.ex_full[e], G::NT * p.R * 2 + (base_tma ? G::NB64 * TM * 128 : 0));
-                tma_load_2d(ys + k.ex_b, &k.tmB, 0, U.w * (int)p.N + x0, &B.ex_full[e]);
+                load_b_rows(k, ys + k.ex_b, U.w, x0, G::NT, &B.ex_full[e]);
                 if (base_tma)
                     for (int bx = 0; bx < G::NB64; ++bx)
                         tma_load_2d(ys + bx * TM * 128, &k.tmY, x0 + 64 * bx, tok[0], &B.ex_full[e]);
@@ -879,6 +900,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) lora_tma_kernel(const __grid_c
         fence_mbar_init();
         prefetch_tmap(&k.tmA);
         prefetch_tmap(&k.tmB);
+        if (k.p.b_tuple)
+            for (int j = 0; j < kMaxSlices; ++j) prefetch_tmap(&k.tmBs[j]);
         if (k.row_tma) {
             prefetch_tmap(&k.tmX);
             prefetch_tmap(&k.tmY);

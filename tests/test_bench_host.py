@@ -24,8 +24,8 @@ SHAPES = {
 
 @pytest.mark.parametrize("name, kernels", [
     ("decode_qkv", 1),         # 32-token tiles, 6144 columns: one fused kernel
-    ("prefill_gate_up", 2),    # 128-token tiles, K = 4096: shrink into the workspace, then expand
-    ("skewed_down_proj", 1),   # K = 14336 is past the two-kernel path's K <= 4096
+    ("prefill_gate_up", 2),    # 128-token tiles: shrink into the workspace, then expand
+    ("skewed_down_proj", 2),   # 128-token tiles, K = 14336: the same two kernels
     ("lm_head_decode", 2),     # 16-token tiles, 128256 columns: the vocabulary-wide split
     ("lm_head_pruned", 2),
     ("tiny", 1),

@@ -56,3 +56,69 @@ def test_embedding_workload_full_size():
     ta = oracle.token_adapter(e.req_lens, e.req_adapter)
     ref, bad = oracle.embedding(e.ids, e.A_emb, ta, e.ranks)
     assert bad == 0 and np.array_equal(out, ref)
+
+
+def _with_extra(e, E, frac, seed):
+    """Replace a fraction of e's ids by extra-token ids in [V, V + E) and draw
+    the slots' extra rows (L, E, R)."""
+    rng = np.random.default_rng(seed)
+    ids = e.ids.copy()
+    pick = rng.random(e.s) < frac
+    ids[pick] = e.V + rng.integers(0, E, size=int(pick.sum()))
+    extra = wl.normal_bf16(rng, (e.L, E, e.R), 0.02)
+    return ids, extra
+
+
+@pytest.mark.parametrize("R,ranks", [(8, [8, 3, 0, 5]), (32, [32, 31, 1, 0]), (40, [40, 0, 17, 39])])
+def test_extra_tokens_bit_exact(R, ranks):
+    e = wl.embedding_gather(seed=R + 1, n_req=7, req_len=45, V=1000, R=R, L=4)
+    e.req_lens = np.array([45, 0, 100, 3, 45, 1, 17], np.int32)
+    e.ids = np.random.default_rng(R).integers(0, 1000, size=e.s).astype(np.int32)
+    e.ranks[:] = ranks
+    ids, extra = _with_extra(e, 9, 0.3, R)
+    bi = build_batch(e)
+    out = torch.full((e.s, e.R), 5.0, dtype=torch.bfloat16, device="cuda")
+    B.embedding_lora_a_extra(dev_i32(ids), dev_bf16(e.A_emb), e.V, dev_bf16(extra), out, bi)
+    torch.cuda.synchronize()
+    assert bi.device_status() == 0
+    ta = oracle.token_adapter(e.req_lens, e.req_adapter)
+    ref, bad = oracle.embedding_extra(ids, e.A_emb, extra, ta, e.ranks)
+    assert bad == 0 and np.array_equal(host_bits(out), ref)
+
+
+def test_extra_tokens_full_size_and_bad_ids():
+    """The 8192-id workload with 64 extra tokens (10 % of ids) bit-exact; then
+    an id past the extra table and a negative id are flagged and zeroed."""
+    e = wl.embedding_gather()
+    ids, extra = _with_extra(e, 64, 0.1, 7)
+    ta = oracle.token_adapter(e.req_lens, e.req_adapter)
+    for bad_ids in (False, True):
+        if bad_ids:
+            ids[[5, 4000]] = [e.V + 64, -3]
+        bi = build_batch(e)
+        out = torch.full((e.s, e.R), 5.0, dtype=torch.bfloat16, device="cuda")
+        B.embedding_lora_a_extra(dev_i32(ids), dev_bf16(e.A_emb), e.V, dev_bf16(extra), out, bi)
+        torch.cuda.synchronize()
+        ref, bad = oracle.embedding_extra(ids, e.A_emb, extra, ta, e.ranks)
+        assert bad == (2 if bad_ids else 0)
+        assert bool(bi.device_status() & 4) == bad_ids
+        assert np.array_equal(host_bits(out), ref)
+
+
+@pytest.mark.parametrize("D", [4096, 100])
+def test_extra_token_embedding_rows(D):
+    """run_extra_token_embedding: rows of extra tokens of an (s, D) output are
+    replaced by their slot's extra rows, every other row keeps its bits."""
+    e = wl.embedding_gather(seed=11, n_req=16, req_len=512 if D == 4096 else 40, V=128256, R=8, L=6)
+    ids, _ = _with_extra(e, 16, 0.05, 3)
+    rng = np.random.default_rng(4)
+    extra = wl.normal_bf16(rng, (e.L, 16, D), 0.5)
+    output = wl.normal_bf16(rng, (e.s, D), 0.5)
+    bi = build_batch(e)
+    y = dev_bf16(output)
+    B.extra_token_embedding(dev_i32(ids), y, dev_bf16(extra), e.V, bi)
+    torch.cuda.synchronize()
+    assert bi.device_status() == 0
+    ta = oracle.token_adapter(e.req_lens, e.req_adapter)
+    ref, bad = oracle.extra_token_embedding(ids, output, extra, e.V, ta)
+    assert bad == 0 and np.array_equal(host_bits(y), ref)
