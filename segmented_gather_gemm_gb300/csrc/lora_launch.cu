@@ -381,8 +381,7 @@ size_t carve_stream(StreamParams &k, int Sy) {
     k.b_slot_bytes = kStCols * k.p.R * 2;
     k.o_bar = take((size_t)(2 * k.Sb + 2 * Sy + 2 * kStAcc + 4) * 8 + 16, 16);
     k.o_run = take((size_t)(5 * k.runcap + 1 + 32) * 4, 16);
-    k.o_tok = take((size_t)(2 * 128 + 4) * 4, 16);
-    k.o_op = take((size_t)4 * kStTileBytes, 1024);
+    k.o_tok = take((size_t)(2 * 128 + 8) * 4, 16);
     k.o_bring = take((size_t)k.Sb * k.b_slot_bytes, 1024);
     k.o_yring = take((size_t)Sy * k.y_slot_bytes, 1024);
     // at least 116 KB, so that one CTA holds an SM (and its 512 TMEM columns)

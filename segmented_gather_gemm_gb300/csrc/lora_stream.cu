@@ -3,6 +3,9 @@
 
 namespace csgmv {
 
+constexpr int kOpLoCol = kStOpCols / 2;  // the lo half of an operand buffer
+constexpr int kStOpBar = 1;              // named barrier of the operand warps
+
 struct StBars {
     uint64_t *b_full, *b_empty;      // [Sb]
     uint64_t *y_full, *y_empty;      // [Sy]
@@ -10,7 +13,7 @@ struct StBars {
     uint64_t *op_full, *op_empty;    // [2]
     uint32_t *tmem_slot;
     int *tok;   // [2][128] token of each tile row (-1: none)
-    int *flag;  // [2] the tile's rows are consecutive tokens; [2, 4) scratch
+    int *flag;  // [2] the tile's rows are consecutive tokens; [2, 6) scratch
 };
 
 __device__ __forceinline__ StBars st_bars(const StreamParams &k, unsigned char *smem) {
@@ -152,7 +155,6 @@ __device__ void st_mma(const StreamParams &k, unsigned char *smem, const int *ta
     const StBars W = st_bars(k, smem);
     const int Rb = p.R * 2;
     const int pcB = p.R / 8, shB = pc_shift_of(pcB);
-    const uint32_t op0 = smem_u32(smem + k.o_op);
     uint32_t g = 0, uc = 0;
     for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
         StUnit U;
@@ -163,7 +165,7 @@ __device__ void st_mma(const StreamParams &k, unsigned char *smem, const int *ta
         tc_fence_after();
         const int RK = (r + 15) & ~15;
         const int ksteps = RK / 16;
-        const uint32_t ahi = op0 + (uint32_t)(2 * b) * kStTileBytes, alo = ahi + kStTileBytes;
+        const uint32_t ahi = tmem + (uint32_t)(kStOpCol0 + b * kStOpCols), alo = ahi + kOpLoCol;
         for (int i = 0; i < U.nt; ++i, ++g) {
             const int sb = g % k.Sb;
             const int a = g % kStAcc;
@@ -191,8 +193,8 @@ __device__ void st_mma(const StreamParams &k, unsigned char *smem, const int *ta
                 const uint32_t d = tmem + (uint32_t)(a * kStCols);
                 for (int ks = 0; ks < ksteps; ++ks) {
                     const uint64_t bd = smem_desc_kmajor(bsa + ks * 32, Rb);
-                    tc_mma_bf16(d, smem_desc_kmajor(ahi + ks * 32, 128), bd, idesc, ks > 0);
-                    tc_mma_bf16(d, smem_desc_kmajor(alo + ks * 32, 128), bd, idesc, true);
+                    tc_mma_bf16_tmem_a(d, ahi + ks * 8, bd, idesc, ks > 0);
+                    tc_mma_bf16_tmem_a(d, alo + ks * 8, bd, idesc, true);
                 }
                 tc_commit(&W.b_empty[sb]);
                 tc_commit(&W.acc_full[a]);
@@ -242,72 +244,60 @@ __device__ __forceinline__ void st_h8(const LoraParams &p, int t, int col, int l
 }
 
 __device__ void st_operands(const StreamParams &k, unsigned char *smem, const int *tables, int nruns,
-                            int64_t nunits) {
+                            int64_t nunits, uint32_t tmem) {
     const LoraParams &p = k.p;
-    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;  // TMEM lanes (tile rows) 32q .. 32q+31
+    const int row = 32 * q + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const StBars W = st_bars(k, smem);
     uint32_t uc = 0;
     for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
         StUnit U;
         int r;
-        if (!st_unit(k, tables, nruns, u, lane == 0, U, r)) continue;
+        if (!st_unit(k, tables, nruns, u, row == 0, U, r)) continue;
         const int b = uc & 1;
         mbar_wait(&W.op_empty[b], ((uc >> 1) & 1) ^ 1, p.status, kStatusTimeout);
         int *tok = W.tok + b * 128;
-        int tm[4];
-#pragma unroll
-        for (int h4 = 0; h4 < 4; ++h4) {  // tile rows lane, lane + 32, ...
-            const int m = lane + 32 * h4;
-            int t = -1;
-            if (m < U.M) {
-                t = p.permutation[U.p0 + m];
-                if (t < 0 || t >= p.num_tokens) {
-                    atomicOr(p.status, CSGMV_STATUS_BAD_PERMUTATION);
-                    t = -1;
-                }
+        int t = -1;
+        if (row < U.M) {
+            t = p.permutation[U.p0 + row];
+            if (t < 0 || t >= p.num_tokens) {
+                atomicOr(p.status, CSGMV_STATUS_BAD_PERMUTATION);
+                t = -1;
             }
-            tok[m] = t;
-            tm[h4] = t;
         }
-        __syncwarp();
+        tok[row] = t;
+        named_bar_sync(kStOpBar, 128);
         const int t0 = tok[0];
-        bool mine = true;
-#pragma unroll
-        for (int h4 = 0; h4 < 4; ++h4) {
-            const int m = lane + 32 * h4;
-            if (m < U.M) mine = mine && tm[h4] == t0 + m;
-        }
-        const bool contig = __all_sync(0xffffffffu, mine) && t0 >= 0;
-        if (lane == 0) W.flag[b] = contig ? 1 : 0;
+        const bool wall = __all_sync(0xffffffffu, row >= U.M || t == t0 + row);
+        if (lane == 0) W.flag[2 + q] = wall ? 1 : 0;
+        named_bar_sync(kStOpBar, 128);
+        if (row == 0) W.flag[b] = (W.flag[2] && W.flag[3] && W.flag[4] && W.flag[5] && t0 >= 0) ? 1 : 0;
 
-        // operand tiles: row m = token m of the tile, columns [0, RK) of slice j
-        unsigned char *ahi = smem + k.o_op + (2 * b) * kStTileBytes;
-        unsigned char *alo = ahi + kStTileBytes;
+        // this row of h (columns [0, RK) of slice j) as bf16 hi / lo pairs
         const int RK = (r + 15) & ~15;
         const int col0 = U.j * r;
+        const uint32_t ob = tmem + lane_base + (uint32_t)(kStOpCol0 + b * kStOpCols);
+        for (int kb = 0; kb < RK / 16; ++kb) {
+            float v[16];
+            if (t >= 0) {
+                float (&v0)[8] = *reinterpret_cast<float (*)[8]>(&v[0]);
+                float (&v1)[8] = *reinterpret_cast<float (*)[8]>(&v[8]);
+                st_h8(p, t, col0 + kb * 16, col0 + r, v0);
+                st_h8(p, t, col0 + kb * 16 + 8, col0 + r, v1);
+            } else {
 #pragma unroll
-        for (int h4 = 0; h4 < 4; ++h4) {
-            const int m = lane + 32 * h4;
-            const int t = tm[h4];
-            for (int ch = 0; ch < RK / 8; ++ch) {
-                float v[8];
-                if (t >= 0) {
-                    st_h8(p, t, col0 + ch * 8, col0 + r, v);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = 0.f;
-                }
-                uint4 hi, lo;
-                split_pair(v[0], v[1], hi.x, lo.x);
-                split_pair(v[2], v[3], hi.y, lo.y);
-                split_pair(v[4], v[5], hi.z, lo.z);
-                split_pair(v[6], v[7], hi.w, lo.w);
-                const int off = m * 128 + ((ch ^ (m & 7)) << 4);
-                *reinterpret_cast<uint4 *>(ahi + off) = hi;
-                *reinterpret_cast<uint4 *>(alo + off) = lo;
+                for (int e = 0; e < 16; ++e) v[e] = 0.f;
             }
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) split_pair(v[2 * e], v[2 * e + 1], hi[e], lo[e]);
+            tmem_st8(ob + (uint32_t)(kb * 8), hi);
+            tmem_st8(ob + (uint32_t)(kOpLoCol + kb * 8), lo);
         }
-        fence_proxy_async_smem();  // the operand tiles are read by the tensor core
+        tmem_wait_st();
+        tc_fence_before();  // the operand columns are read by the tensor core
         __syncwarp();
         if (lane == 0) mbar_arrive(&W.op_full[b]);
         ++uc;
@@ -428,7 +418,7 @@ __global__ void __launch_bounds__(kStThreads, 1) lora_stream_expand_kernel(const
             mbar_init(&W.acc_empty[i], 4);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&W.op_full[i], 1);
+            mbar_init(&W.op_full[i], 4);                 // the operand warps
             mbar_init(&W.op_empty[i], 1 + kStEpiWarps);  // producer + epilogue warps
         }
         fence_mbar_init();
@@ -450,9 +440,9 @@ __global__ void __launch_bounds__(kStThreads, 1) lora_stream_expand_kernel(const
     const int64_t nunits = (int64_t)ntiles * k.upt;
     if (warp == 0) st_producer(k, smem, tables, nruns, nunits);
     else if (warp == 1) st_mma(k, smem, tables, nruns, nunits, tmem);
-    else if (warp == 2) st_operands(k, smem, tables, nruns, nunits);
-    else if (warp == 3) st_b_producer(k, smem, tables, nruns, nunits);
-    else st_epilogue(k, smem, tables, nruns, nunits, tmem);
+    else if (warp == 2) st_b_producer(k, smem, tables, nruns, nunits);
+    else if (warp >= kStOpWarp0 && warp < kStEpiWarp0) st_operands(k, smem, tables, nruns, nunits, tmem);
+    else if (warp >= kStEpiWarp0) st_epilogue(k, smem, tables, nruns, nunits, tmem);
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

@@ -15,15 +15,16 @@
 //               rows (128-row TMA boxes when the tile's tokens are
 //               consecutive, else TMA 4-row gathers) into a ring of base
 //               slots;
-//   warp 3      B producer: per stage, the slot's B rows (one TMA box per 64
+//   warp 2      B producer: per stage, the slot's B rows (one TMA box per 64
 //               columns) into a ring of B slots, running ahead of the rest;
 //   warp 1      MMA issuer: per stage, y_delta = h B^T on the tensor cores
 //               (h as a bf16 hi + lo pair, so it keeps ~16 bits) into one of
 //               kStAcc TMEM accumulators; completions free the B slot;
-//   warp 2      operands: per unit, the token list and h of the unit's slice
-//               from global memory as bf16 hi / lo operand tiles (128-byte
-//               swizzle), double-buffered one unit ahead;
-//   warps 4..   epilogue, teams of four warps that take the stages in turn: each
+//   warps 4-7   operands: per unit, the token list and h of the unit's slice
+//               from global memory as bf16 hi / lo pairs written into TMEM
+//               (each warp its lane quarter), where the MMA takes them as its A
+//               operand; double-buffered one unit ahead;
+//   warps 8..   epilogue, teams of four warps that take the stages in turn: each
 //               warp reads its 32 accumulator rows (tcgen05.ld), adds base in
 //               fp32 and writes the rounded rows back in place, then stores
 //               its 32-row piece with TMA box stores (a full tile of
@@ -36,22 +37,29 @@
 
 namespace csgmv {
 
-constexpr int kStTeams = 3;              // epilogue teams of four warps, taking stages in turn
+constexpr int kStTeams = 2;              // epilogue teams of four warps, taking stages in turn
+constexpr int kStOpWarp0 = 4;            // four operand warps, one TMEM lane quarter each
+constexpr int kStEpiWarp0 = 8;
 constexpr int kStEpiWarps = 4 * kStTeams;
-constexpr int kStWarps = 4 + kStEpiWarps;
+constexpr int kStWarps = kStEpiWarp0 + kStEpiWarps;
 constexpr int kStThreads = kStWarps * 32;
 constexpr int kStBoxes = 1;              // 64-column boxes per stage
 constexpr int kStCols = 64 * kStBoxes;   // output columns per stage
-// TMEM accumulators of kStCols columns.  Every mbarrier of the epilogue is
-// waited on by one team only: stage g takes accumulator g % kStAcc, base slot
-// g % Sy and team g % kStTeams, so kStAcc and Sy are multiples of kStTeams (a
-// team that waited on a barrier another team also waits on could take a
-// phase two completions old for the current one).
 constexpr int kStTmemCols = 512;         // the allocation: a power of two
-constexpr int kStAcc = (kStTmemCols / kStCols) / kStTeams * kStTeams;
-constexpr int kStTileBytes = 128 * 128;  // 128 rows x 64 bf16: one base box or an operand tile
-constexpr int kStBSlots = 4;             // B tiles in flight (needed only until their MMAs are done)
-constexpr int kStEpiWarp0 = 4;
+// h of a unit in TMEM as the MMA's A operand: rows in lanes, two bf16 of
+// consecutive K per 32-bit column; the hi half in columns [0, 32) and the lo
+// half in [32, 64) of an operand buffer, two buffers at the top of TMEM.
+constexpr int kStOpCols = 64;
+constexpr int kStOpCol0 = kStTmemCols - 2 * kStOpCols;
+// TMEM accumulators of kStCols columns below the operand buffers.  Every
+// mbarrier of the epilogue is waited on by one team only: stage g takes
+// accumulator g % kStAcc, base slot g % Sy and team g % kStTeams, so kStAcc
+// and Sy are multiples of kStTeams (a team that waited on a barrier another
+// team also waits on could take a phase two completions old for the current
+// one).
+constexpr int kStAcc = (kStOpCol0 / kStCols) / kStTeams * kStTeams;
+constexpr int kStTileBytes = 128 * 128;  // 128 rows x 64 bf16: one base box
+constexpr int kStBSlots = 6;             // B tiles in flight (needed only until their MMAs are done)
 static_assert(kStAcc >= kStTeams, "every team needs an accumulator");
 
 struct StreamParams {
@@ -64,7 +72,7 @@ struct StreamParams {
     int cb;                       // columns of a unit (multiple of 64)
     int upt;                      // units per tile: sum over slices of ceil(width / cb)
     int Sy, Sb;                   // base slots, B slots
-    int o_bar, o_run, o_tok, o_op, o_yring, o_bring;
+    int o_bar, o_run, o_tok, o_yring, o_bring;
     int y_slot_bytes, b_slot_bytes;  // kStBoxes base boxes; kStCols rows of B
 };
 
