@@ -380,7 +380,7 @@ size_t carve_stream(StreamParams &k, int Sy) {
     k.y_slot_bytes = kStBoxes * kStTileBytes;
     k.b_slot_bytes = kStCols * k.p.R * 2;
     k.o_bar = take((size_t)(2 * k.Sb + 2 * Sy + 2 * kStAcc + 4) * 8 + 16, 16);
-    k.o_run = take((size_t)(5 * k.runcap + 1 + 32) * 4, 16);
+    k.o_run = take((size_t)(8 * k.runcap + 1 + 32) * 4, 16);  // run table cut at token gaps
     k.o_tok = take((size_t)(2 * 128 + 8) * 4, 16);
     k.o_bring = take((size_t)k.Sb * k.b_slot_bytes, 1024);
     k.o_yring = take((size_t)Sy * k.y_slot_bytes, 1024);
@@ -400,7 +400,7 @@ size_t carve_sshrink(ShrinkParams &k, int S) {
     k.S = S;
     k.stage_bytes = (int)align_up((size_t)128 * 128 + align_up((size_t)k.p.c * k.p.R, 16) * 128, 1024);
     k.o_bar = take((size_t)(2 * S + 6) * 8 + 16, 16);
-    k.o_run = take((size_t)(5 * k.runcap + 1 + 32) * 4, 16);
+    k.o_run = take((size_t)(8 * k.runcap + 1 + 32) * 4, 16);  // run table cut at token gaps
     k.o_tok = take((size_t)(2 * 128 + 2) * 4, 16);
     k.o_ring = take((size_t)S * k.stage_bytes, 1024);
     return std::max(off + 1024, (size_t)116 * 1024);

@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kShThreads, 1) lora_stream_shrink_kernel(const
     tc_fence_before();
     int nruns = 0;
     int *tables = reinterpret_cast<int *>(smem + k.o_run);
-    const int ntiles = build_run_table_raw<128>(k.p, k.max_segments, k.runcap, tables, &nruns);  // ends with __syncthreads
+    const int ntiles = build_run_table_raw<128, true>(k.p, k.max_segments, k.runcap, tables, &nruns);  // ends with __syncthreads
     tc_fence_after();
     const uint32_t tmem = *W.tmem_slot;
     const int64_t nunits = (int64_t)ntiles * k.P;

@@ -135,10 +135,85 @@ __device__ __forceinline__ int block_scan(int v, int *scratch, int *total) {
     return pre;
 }
 
+// Cuts the slot runs (starts run_p0, ends run_end, slots run_w; adjacent and
+// in position order) where the permutation is not consecutive; the cut runs
+// replace them in the same arrays.  Each thread scans 16 positions per pass;
+// the break positions are placed by a block scan.  `scratch` is followed by
+// 3 * runcap ints of room.  Returns the new run count (0 and a status bit on
+// overflow).  Every thread of the block calls it.
+static __device__ __noinline__ int split_runs_at_gaps(const LoraParams &p, int runcap, int *run_p0, int *run_end,
+                                               int *run_w, int *scratch, int nruns) {
+    constexpr int PT = 16;
+    int *sub_p0 = scratch + 32, *sub_w = sub_p0 + runcap, *sub_end = sub_w + runcap;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int first = nruns > 0 ? run_p0[0] : 0, last = nruns > 0 ? run_end[nruns - 1] : 0;
+    int nsub = 0;
+    for (int base = first; base < last; base += nt * PT) {
+        const int a = base + tid * PT;
+        int r = 0;  // the run holding position a
+        {
+            int lo = 0, hi = nruns;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (run_p0[mid] <= a) lo = mid; else hi = mid;
+            }
+            r = lo;
+        }
+        uint32_t brk = 0;
+        int prev = a > 0 ? p.permutation[a - 1] : -2;
+        int rr = r;
+#pragma unroll
+        for (int i = 0; i < PT; ++i) {
+            const int pp = a + i;
+            if (pp < last) {
+                while (rr + 1 < nruns && run_p0[rr + 1] <= pp) ++rr;
+                const int v = p.permutation[pp];
+                if (pp == run_p0[rr] || v != prev + 1) brk |= 1u << i;
+                prev = v;
+            }
+        }
+        int tot;
+        const int pre = block_scan(__popc(brk), scratch, &tot);
+        int idx = nsub + pre;
+        rr = r;
+        for (int i = 0; i < PT; ++i) {
+            if (!((brk >> i) & 1u)) continue;
+            const int pp = a + i;
+            while (rr + 1 < nruns && run_p0[rr + 1] <= pp) ++rr;
+            if (idx < runcap) {
+                sub_p0[idx] = pp;
+                sub_w[idx] = run_w[rr];
+                sub_end[idx] = run_end[rr];
+            }
+            ++idx;
+        }
+        nsub += tot;
+    }
+    if (nsub > runcap) {
+        if (tid == 0) atomicOr(p.status, CSGMV_STATUS_CAPACITY);
+        nsub = 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < nsub; i += nt) {
+        run_p0[i] = sub_p0[i];
+        run_w[i] = sub_w[i];
+        run_end[i] = i + 1 < nsub ? min(sub_p0[i + 1], sub_end[i]) : sub_end[i];
+    }
+    __syncthreads();
+    return nsub;
+}
+
 // Slot runs of the batch info and their token tiles (see the file comment).
 // Returns the number of tiles; the tables live in shared memory.
-// `tables` holds 5 * runcap + 1 + 32 ints; every thread of the block calls it.
-template <int TM>
+// `tables` holds 5 * runcap + 1 + 32 ints (8 * runcap + 1 + 32 with SPLIT);
+// every thread of the block calls it.
+//
+// SPLIT: runs are also cut wherever the permutation is not consecutive
+// (permutation[p] != permutation[p-1] + 1, i.e. between two requests on one
+// slot), so every tile holds consecutive tokens and moves its rows as TMA
+// boxes.  A request's tokens stay together in the stable sort, so this gives
+// at most one run per request: the run capacity max_bs + max_loras holds.
+template <int TM, bool SPLIT = false>
 __device__ int build_run_table_raw(const LoraParams &p, int max_segments, int runcap, int *tables,
                                    int *nruns_out) {
     int *run_seg = tables;
@@ -183,6 +258,7 @@ __device__ int build_run_table_raw(const LoraParams &p, int max_segments, int ru
         nruns = 0;
     }
     __syncthreads();
+    if constexpr (SPLIT) nruns = split_runs_at_gaps(p, runcap, run_p0, run_len, run_w, scratch, nruns);
     int tcarry = 0;
     for (int r0 = 0; r0 < nruns; r0 += nt) {
         const int r = r0 + tid;
