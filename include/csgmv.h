@@ -219,9 +219,9 @@ CSGMV_API int csgmv_expand(const void *h, int h_dtype, int64_t ldh, const void *
  *   workspace, workspace_bytes   optional device scratch for h (NULL / 0 for
  *       none).  Without it h never leaves the chip (reduced across a
  *       thread-block cluster in distributed shared memory).  With room for
- *       at least one plane of fp32 h (num_tokens * num_slices * max_rank * 4
- *       bytes; csgmv_qkv_workspace_bytes() covers every batch and the widest
- *       split of K), two kinds of call instead run the shrink and the expand
+ *       a 256-byte header and one plane of fp32 h (num_tokens * num_slices *
+ *       max_rank * 4 bytes; csgmv_qkv_workspace_bytes() covers every batch
+ *       and the widest split of K), two kinds of call instead run the shrink and the expand
  *       as two kernels with h in the workspace, which is faster there:
  *       batches of long per-slot runs (128-token tiles, max_rank >= 16; the
  *       shrink may cut K into parts, one plane of partial sums each, that the
@@ -256,9 +256,9 @@ CSGMV_API int csgmv_qkv_sliced(const void *x, int64_t K, const void *A, const vo
 
 /* Workspace bytes that let csgmv_qkv use its two-kernel path for any batch
  * of this batch info, with h (fp32) held as up to four partial sums over parts
- * of K: 4 * max_tokens * num_slices * max_rank * 4.  A smaller workspace of at
- * least max_tokens * num_slices * max_rank * 4 bytes also takes the path, with
- * fewer parts. */
+ * of K after a 256-byte header: 256 + 4 * max_tokens * num_slices * max_rank
+ * * 4.  A smaller workspace of at least 256 + num_tokens * num_slices *
+ * max_rank * 4 bytes also takes the path, with fewer parts. */
 CSGMV_API size_t csgmv_qkv_workspace_bytes(const csgmv_batch_info *bi, int num_slices);
 
 /*
@@ -271,7 +271,8 @@ CSGMV_API size_t csgmv_qkv_workspace_bytes(const csgmv_batch_info *bi, int num_s
  * library's own device memory as the h workspace; the library allocates
  * nothing and frees nothing here either.
  *   - Limit: the batch's h, num_tokens * num_slices * max_rank * 4 bytes,
- *     must fit in 32 MiB, else CSGMV_ERR_CAPACITY (nothing is launched).
+ *     and a 256-byte header must fit in 32 MiB, else CSGMV_ERR_CAPACITY
+ *     (nothing is launched).
  *   - Every GPU that loads the library holds the 32 MiB until the process
  *     exits.
  *   - The first call on each device looks up the array's device address

@@ -112,6 +112,7 @@ void single_b(csgmv::LoraParams &p) {
 void fill_common(csgmv::LoraParams &p, const csgmv_batch_info *bi) {
     p.h_parts = 1;
     p.h_plane = 0;
+    p.h_parts_dev = nullptr;
     p.seg_indptr = bi->seg_indptr;
     p.weight_indices = bi->weight_indices;
     p.permutation = bi->permutation;
@@ -223,9 +224,9 @@ int qkv_impl(const void *x, int64_t K, const void *A, const void *B, const void 
     set_b(p, B_slices);
     p.accumulate = 1;
     const size_t hbytes = (size_t)s * num_slices * bi->max_rank * 4;
-    if (workspace && workspace_bytes >= hbytes && csgmv::qkv_split_pays(p, *bi)) {
-        // the planes of h the call may write: up to kMaxKParts of hbytes
-        const size_t ws_used = std::min(workspace_bytes, (size_t)csgmv::kMaxKParts * hbytes);
+    if (workspace && workspace_bytes >= csgmv::kWsHeader + hbytes && csgmv::qkv_split_pays(p, *bi)) {
+        // the header and the planes of h the call may write: up to kMaxKParts of hbytes
+        const size_t ws_used = std::min(workspace_bytes, csgmv::kWsHeader + (size_t)csgmv::kMaxKParts * hbytes);
         if (!aligned16(workspace)) return fail(CSGMV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
         if (overlaps_batch_info(bi, workspace, ws_used) ||
             overlaps(workspace, ws_used, base_output, (size_t)s * N * 2))
@@ -247,7 +248,8 @@ int qkv_impl(const void *x, int64_t K, const void *A, const void *B, const void 
         pe.h = workspace;
         pe.h_f32 = 1;
         pe.ldh = ps.ldh;
-        cudaError_t e = csgmv::launch_qkv_split(ps, pe, *bi, reinterpret_cast<cudaStream_t>(stream), ws_used);
+        cudaError_t e =
+            csgmv::launch_qkv_split(ps, pe, *bi, reinterpret_cast<cudaStream_t>(stream), workspace, ws_used);
         if (e != cudaSuccess) return cuda_fail(e, "csgmv_qkv shrink / expand launch");
         return CSGMV_OK;
     }
@@ -413,7 +415,7 @@ int csgmv_expand_sliced(const void *h, int h_dtype, int64_t ldh, const void *con
 
 size_t csgmv_qkv_workspace_bytes(const csgmv_batch_info *bi, int num_slices) {
     if (!bi || bi->max_tokens < 0 || bi->max_rank < 0 || num_slices < 1 || num_slices > csgmv::kMaxSlices) return 0;
-    return (size_t)csgmv::kMaxKParts * bi->max_tokens * num_slices * bi->max_rank * 4;
+    return csgmv::kWsHeader + (size_t)csgmv::kMaxKParts * bi->max_tokens * num_slices * bi->max_rank * 4;
 }
 
 int csgmv_qkv(const void *x, int64_t K, const void *A, const void *B, int64_t N, const int32_t *slice_offsets,

@@ -12,6 +12,7 @@ constexpr int kMaxRank = 64;       // largest buffer rank R the LoRA kernels tak
 constexpr int kMaxSlices = 3;
 constexpr int kWideCols = 32768;   // output columns from which 16- / 32-token csgmv_qkv calls split
 constexpr int kMaxKParts = 4;      // fp32 h planes of the csgmv_qkv workspace (parts of K)
+constexpr size_t kWsHeader = 256;  // bytes before the planes: the part count the shrink chose
 
 #ifdef __CUDACC__
 // Programmatic dependent launch.  A kernel launched with
@@ -49,6 +50,7 @@ struct LoraParams {
     // apart (the csgmv_qkv workspace path); 1 = h itself
     int h_parts;
     int64_t h_plane;
+    const int *h_parts_dev;  // the part count as the shrink chose it (read on the device, <= h_parts), or NULL
     int h_f32;
     int c, R;
     int off[kMaxSlices + 1];
@@ -84,11 +86,12 @@ int set_error(int code, const char *msg);
 
 // Whether csgmv_qkv should run as shrink + expand through a workspace.
 bool qkv_split_pays(const LoraParams &p, const csgmv_batch_info &bi);
-// csgmv_qkv's two-kernel path: shrink (ps) into the fp32 workspace, as up to
-// workspace_bytes / (s * c * R * 4) partial-sum planes over parts of K, then
-// the expand (pe) from it.
+// csgmv_qkv's two-kernel path: shrink (ps) into the fp32 workspace (a
+// kWsHeader-byte header, then up to (workspace_bytes - kWsHeader) /
+// (s * c * R * 4) partial-sum planes over parts of K), then the expand (pe)
+// from it.
 cudaError_t launch_qkv_split(LoraParams &ps, LoraParams &pe, const csgmv_batch_info &bi, cudaStream_t stream,
-                             size_t workspace_bytes);
+                             void *workspace, size_t workspace_bytes);
 
 // builder.cu
 struct BuildParams {

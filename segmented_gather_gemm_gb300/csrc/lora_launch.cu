@@ -407,11 +407,12 @@ size_t carve_sshrink(ShrinkParams &k, int S) {
 }
 
 // Shrink on 128-token tiles: the streaming tcgen05 kernel, one CTA per SM.
-// K is cut into P <= max_parts parts (P > 1 only into an fp32 workspace of
-// max_parts planes of p.h_plane elements), chosen so that the units fill the
-// CTAs' last wave best; *parts_out gets P.
+// K may be cut into up to max_parts parts (more than one only into an fp32
+// workspace of max_parts planes of p.h_plane elements); the kernel picks the
+// count from the exact tile count and writes it to *parts_dev (device) when
+// that is not NULL.
 cudaError_t launch_lora_sshrink(LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream, LaunchInfo *info,
-                                int max_parts, int *parts_out) {
+                                int max_parts, int *parts_dev) {
     const void *fn = lora_kernel_sshrink();
     cudaError_t e = encoder();  // the tensor-map encoder, resolved on first use
     if (e != cudaSuccess) return e;
@@ -436,27 +437,12 @@ cudaError_t launch_lora_sshrink(LoraParams &p, const csgmv_batch_info &bi, cudaS
     if (res < 1) return cudaErrorInvalidConfiguration;
 
     const int s = p.num_tokens;
-    const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
-    const int tiles_est = std::max(1, (s + 127) / 128 + slots / 2);
-    const int tiles_ub = (s + 127) / 128 + std::min(std::max(bi.bs, 1), std::max(bi.max_loras, 1));
-    const int nkc = (int)((p.K + 63) / 64);
-    // parts of K: the best-filled last wave of units, at least four K chunks a part
-    int best_P = 1;
-    double best_fill = 0.0;
-    for (int P = 1; P <= std::max(1, max_parts); ++P) {
-        const int kc = (nkc + P - 1) / P;
-        const int Pe = (nkc + kc - 1) / kc;
-        if (Pe != P || (P > 1 && kc < 4)) continue;
-        const int64_t units = (int64_t)tiles_est * P;
-        const int64_t waves = (units + res - 1) / res;
-        const double fill = (double)units / (double)(waves * res);
-        if (fill > best_fill + 0.02) { best_fill = fill; best_P = P; }
-    }
-    k.P = best_P;
-    k.kc_per = (nkc + best_P - 1) / best_P;
+    // tiles: one per 128 tokens, plus a partial one per slot run and per request
+    const int tiles_ub = (s + 127) / 128 + std::max(bi.bs, 1) + std::min(std::max(bi.bs, 1), std::max(bi.max_loras, 1));
+    k.max_parts = std::max(1, max_parts);
+    k.parts_out = parts_dev;
     k.plane = p.h_plane;
-    if (parts_out) *parts_out = best_P;
-    const int64_t units_ub = (int64_t)tiles_ub * best_P;
+    const int64_t units_ub = (int64_t)tiles_ub * k.max_parts;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(res, units_ub));
 
     const int L = bi.max_loras;
@@ -591,21 +577,28 @@ bool qkv_split_pays(const LoraParams &p, const csgmv_batch_info &bi) {
 }
 
 cudaError_t launch_qkv_split(LoraParams &ps, LoraParams &pe, const csgmv_batch_info &bi, cudaStream_t stream,
-                             size_t workspace_bytes) {
-    // parts of K the workspace holds (planes of s * c * R floats)
+                             void *workspace, size_t workspace_bytes) {
+    // the workspace: a header (the part count), then planes of s * c * R floats
+    int *header = static_cast<int *>(workspace);
+    float *planes = reinterpret_cast<float *>(static_cast<char *>(workspace) + kWsHeader);
     const size_t plane = (size_t)ps.num_tokens * ps.ldh;
-    int max_parts = (int)std::min<size_t>(kMaxKParts, plane ? workspace_bytes / (plane * 4) : 1);
+    const size_t room = workspace_bytes > kWsHeader ? workspace_bytes - kWsHeader : 0;
+    const int max_parts = (int)std::max<size_t>(1, std::min<size_t>(kMaxKParts, plane ? room / (plane * 4) : 1));
+    ps.h = planes;
+    pe.h = planes;
+    pe.h_plane = (int64_t)plane;
     cudaError_t e;
-    int parts = 1;
     if (token_tile(ps, bi) == 128 && ps.R >= 16) {
         ps.h_plane = (int64_t)plane;
-        e = launch_lora_sshrink(ps, bi, stream, nullptr, std::max(1, max_parts), &parts);
+        e = launch_lora_sshrink(ps, bi, stream, nullptr, max_parts, header);
+        pe.h_parts = max_parts;
+        pe.h_parts_dev = header;
     } else {
         e = launch_lora(kModeShrink, ps, bi, stream, nullptr);
+        pe.h_parts = 1;
+        pe.h_parts_dev = nullptr;
     }
     if (e != cudaSuccess) return e;
-    pe.h_parts = parts;
-    pe.h_plane = (int64_t)plane;
     return launch_lora(kModeExpand, pe, bi, stream, nullptr);
 }
 

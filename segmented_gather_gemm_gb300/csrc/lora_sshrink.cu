@@ -34,20 +34,46 @@ constexpr int kShAccCols = 256;  // TMEM columns per accumulator (c * R <= 192)
 // Unit u of the walk: part u / ntiles of K (so that the CTAs working at one
 // time share the A columns of one part) of token tile u % ntiles.  False when
 // the unit has no tensor-core work (rank 0, an invalid slot or rank).
-__device__ __forceinline__ bool sh_unit(const ShrinkParams &k, const int *tables, int nruns, int ntiles, int64_t u,
-                                        bool report, Unit &T, int &r, int &part, int &c0, int &c1) {
-    part = (int)(u / ntiles);
-    const int tile = (int)(u % ntiles);
+struct ShWalk {
+    int ntiles, P, kc_per;  // tiles, parts of K, 64-wide K chunks per part
+};
+
+__device__ __forceinline__ bool sh_unit(const ShrinkParams &k, const int *tables, int nruns, const ShWalk &wk,
+                                        int64_t u, bool report, Unit &T, int &r, int &part, int &c0, int &c1) {
+    part = (int)(u / wk.ntiles);
+    const int tile = (int)(u % wk.ntiles);
     T = tile_of<128>(tables, k.runcap, nruns, tile);
     r = unit_rank(k.p, T, report && part == 0);
     const int nkc = (int)((k.p.K + 63) / 64);
-    c0 = part * k.kc_per;
-    c1 = min(nkc, c0 + k.kc_per);
+    c0 = part * wk.kc_per;
+    c1 = min(nkc, c0 + wk.kc_per);
     return r > 0 && c1 > c0;
 }
 
+// Parts of K for ntiles tiles on `grid` CTAs: the best-filled last wave, at
+// least four K chunks a part, at most max_parts.  The same on every thread.
+__device__ __forceinline__ ShWalk sh_walk(int ntiles, int nkc, int max_parts, int grid) {
+    ShWalk wk;
+    wk.ntiles = ntiles;
+    wk.P = 1;
+    float best = 0.f;
+    for (int P = 1; P <= max(1, max_parts); ++P) {
+        const int kc = (nkc + P - 1) / P;
+        if ((nkc + kc - 1) / kc != P || (P > 1 && kc < 4)) continue;
+        const long long units = (long long)ntiles * P;
+        const long long waves = (units + grid - 1) / grid;
+        const float fill = (float)units / (float)(waves * grid);
+        if (fill > best + 0.02f) {
+            best = fill;
+            wk.P = P;
+        }
+    }
+    wk.kc_per = (nkc + wk.P - 1) / wk.P;
+    return wk;
+}
+
 // ------------------------------------------------------------------------------------- producer
-__device__ void sh_producer(const ShrinkParams &k, unsigned char *smem, const int *tables, int nruns, int ntiles,
+__device__ void sh_producer(const ShrinkParams &k, unsigned char *smem, const int *tables, int nruns, const ShWalk &wk,
                             int64_t nunits) {
     const LoraParams &p = k.p;
     const int lane = threadIdx.x & 31;
@@ -57,7 +83,7 @@ __device__ void sh_producer(const ShrinkParams &k, unsigned char *smem, const in
     for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
         Unit T;
         int r, part, c0, c1;
-        if (!sh_unit(k, tables, nruns, ntiles, u, lane == 0, T, r, part, c0, c1)) continue;
+        if (!sh_unit(k, tables, nruns, wk, u, lane == 0, T, r, part, c0, c1)) continue;
         const int b = uc & 1;
         mbar_wait(&W.tok_empty[b], ((uc >> 1) & 1) ^ 1, p.status, kStatusTimeout);
         int *tok = W.tok + b * 128;
@@ -112,7 +138,7 @@ __device__ void sh_producer(const ShrinkParams &k, unsigned char *smem, const in
 }
 
 // ------------------------------------------------------------------------------------- MMA issuer
-__device__ void sh_mma(const ShrinkParams &k, unsigned char *smem, const int *tables, int nruns, int ntiles,
+__device__ void sh_mma(const ShrinkParams &k, unsigned char *smem, const int *tables, int nruns, const ShWalk &wk,
                        int64_t nunits, uint32_t tmem) {
     const LoraParams &p = k.p;
     const int lane = threadIdx.x & 31;
@@ -121,7 +147,7 @@ __device__ void sh_mma(const ShrinkParams &k, unsigned char *smem, const int *ta
     for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
         Unit T;
         int r, part, c0, c1;
-        if (!sh_unit(k, tables, nruns, ntiles, u, false, T, r, part, c0, c1)) continue;
+        if (!sh_unit(k, tables, nruns, wk, u, false, T, r, part, c0, c1)) continue;
         const int b = uc & 1;
         mbar_wait(&W.acc_empty[b], ((uc >> 1) & 1) ^ 1, p.status, kStatusTimeout);
         tc_fence_after();
@@ -160,7 +186,7 @@ __device__ __forceinline__ void sh_store(const ShrinkParams &k, int part, int t,
     else reinterpret_cast<__nv_bfloat16 *>(p.h)[o] = __float2bfloat16_rn(v);
 }
 
-__device__ void sh_epilogue(const ShrinkParams &k, unsigned char *smem, const int *tables, int nruns, int ntiles,
+__device__ void sh_epilogue(const ShrinkParams &k, unsigned char *smem, const int *tables, int nruns, const ShWalk &wk,
                             int64_t nunits, uint32_t tmem) {
     const LoraParams &p = k.p;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -173,9 +199,9 @@ __device__ void sh_epilogue(const ShrinkParams &k, unsigned char *smem, const in
     for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
         Unit T;
         int r, part, c0, c1;
-        if (!sh_unit(k, tables, nruns, ntiles, u, false, T, r, part, c0, c1)) {
+        if (!sh_unit(k, tables, nruns, wk, u, false, T, r, part, c0, c1)) {
             // h itself (one part): rows of rank-0 tokens are zero
-            if (r == 0 && k.P == 1 && row < T.M) {
+            if (r == 0 && wk.P == 1 && row < T.M) {
                 const int t = p.permutation[T.p0 + row];
                 if (t >= 0 && t < p.num_tokens)
                     for (int col = 0; col < cR; ++col) sh_store(k, 0, t, col, 0.f);
@@ -208,7 +234,7 @@ __device__ void sh_epilogue(const ShrinkParams &k, unsigned char *smem, const in
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&W.acc_empty[b]);
-        if (k.P == 1 && trow >= 0)  // h itself: columns [c*r, c*R) are zero
+        if (wk.P == 1 && trow >= 0)  // h itself: columns [c*r, c*R) are zero
             for (int col = cr; col < cR; ++col) sh_store(k, 0, trow, col, 0.f);
         __syncwarp();
         if (lane == 0) mbar_arrive(&W.tok_empty[b]);
@@ -248,10 +274,12 @@ __global__ void __launch_bounds__(kShThreads, 1) lora_stream_shrink_kernel(const
     const int ntiles = build_run_table_raw<128, true>(k.p, k.max_segments, k.runcap, tables, &nruns);  // ends with __syncthreads
     tc_fence_after();
     const uint32_t tmem = *W.tmem_slot;
-    const int64_t nunits = (int64_t)ntiles * k.P;
-    if (warp == 0) sh_producer(k, smem, tables, nruns, ntiles, nunits);
-    else if (warp == 1) sh_mma(k, smem, tables, nruns, ntiles, nunits, tmem);
-    else sh_epilogue(k, smem, tables, nruns, ntiles, nunits, tmem);
+    const ShWalk wk = sh_walk(ntiles, (int)((k.p.K + 63) / 64), k.max_parts, gridDim.x);
+    if (k.parts_out && blockIdx.x == 0 && threadIdx.x == 0) *k.parts_out = wk.P;  // for the expand
+    const int64_t nunits = (int64_t)ntiles * wk.P;
+    if (warp == 0) sh_producer(k, smem, tables, nruns, wk, nunits);
+    else if (warp == 1) sh_mma(k, smem, tables, nruns, wk, nunits, tmem);
+    else sh_epilogue(k, smem, tables, nruns, wk, nunits, tmem);
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

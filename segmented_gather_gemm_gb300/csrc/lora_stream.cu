@@ -211,12 +211,12 @@ __device__ void st_mma(const StreamParams &k, unsigned char *smem, const int *ta
 // ------------------------------------------------------------------------------------- operands
 // h[t][col .. col+7] as fp32 (0 past `r` columns of the slice, i.e. col >= lim).
 // fp32 h held as partial sums over parts of K is summed part by part, in order.
-__device__ __forceinline__ void st_h8(const LoraParams &p, int t, int col, int lim, float (&v)[8]) {
+__device__ __forceinline__ void st_h8(const LoraParams &p, int parts, int t, int col, int lim, float (&v)[8]) {
     const int64_t o = (int64_t)t * p.ldh + col;
     if (p.h_f32) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] = 0.f;
-        for (int part = 0; part < p.h_parts; ++part) {
+        for (int part = 0; part < parts; ++part) {
             const float *h = reinterpret_cast<const float *>(p.h) + part * p.h_plane + o;
             if (col + 8 <= lim && ((o + part * p.h_plane) & 3) == 0) {
                 const float4 a = *reinterpret_cast<const float4 *>(h), b = *reinterpret_cast<const float4 *>(h + 4);
@@ -251,6 +251,8 @@ __device__ void st_operands(const StreamParams &k, unsigned char *smem, const in
     const int row = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const StBars W = st_bars(k, smem);
+    // partial-sum planes of h: as the shrink chose them (at most h_parts)
+    const int parts = p.h_parts_dev ? max(1, min(*p.h_parts_dev, p.h_parts)) : p.h_parts;
     uint32_t uc = 0;
     for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
         StUnit U;
@@ -284,8 +286,8 @@ __device__ void st_operands(const StreamParams &k, unsigned char *smem, const in
             if (t >= 0) {
                 float (&v0)[8] = *reinterpret_cast<float (*)[8]>(&v[0]);
                 float (&v1)[8] = *reinterpret_cast<float (*)[8]>(&v[8]);
-                st_h8(p, t, col0 + kb * 16, col0 + r, v0);
-                st_h8(p, t, col0 + kb * 16 + 8, col0 + r, v1);
+                st_h8(p, parts, t, col0 + kb * 16, col0 + r, v0);
+                st_h8(p, parts, t, col0 + kb * 16 + 8, col0 + r, v1);
             } else {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) v[e] = 0.f;

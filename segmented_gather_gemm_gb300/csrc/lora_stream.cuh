@@ -89,9 +89,12 @@ struct StreamParams {
 //               one is written out);
 //   warps 2-5   epilogue: each warp its 32 rows of the accumulator
 //               (tcgen05.ld), written as fp32 (or bf16) h rows.
-// With P > 1 (the csgmv_qkv workspace path) part p of K goes to plane p of
-// the workspace and the expand sums the planes in order; P = 1 writes h
-// itself, with zeros in columns [c*r, c*R) and in rows of rank-0 tokens.
+// The part count P is chosen on the device from the exact tile count (the
+// best-filled last wave, at most max_parts).  With P > 1 (the csgmv_qkv
+// workspace path) part p of K goes to plane p of the workspace, P is written
+// to the workspace header, and the expand sums the planes in order; P = 1
+// writes h itself, with zeros in columns [c*r, c*R) and in rows of rank-0
+// tokens.
 constexpr int kShWarps = 6;
 constexpr int kShThreads = kShWarps * 32;
 constexpr int kShEpiWarp0 = 2;
@@ -102,8 +105,8 @@ struct ShrinkParams {
     CUtensorMap tmA;   // A (L * c * R rows, K): box 64 x 16, 128-byte swizzle
     LoraParams p;
     int runcap, max_segments;
-    int P;             // parts of K
-    int kc_per;        // 64-wide K chunks per part
+    int max_parts;     // parts of K the output holds (1: h itself)
+    int *parts_out;    // where the chosen part count goes (the workspace header), or NULL
     int S;             // ring stages
     int o_bar, o_run, o_tok, o_ring;
     int stage_bytes;   // x tile + A tile of round16(c * R) rows

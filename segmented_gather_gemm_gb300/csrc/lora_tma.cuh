@@ -137,19 +137,31 @@ __device__ __forceinline__ int block_scan(int v, int *scratch, int *total) {
 
 // Cuts the slot runs (starts run_p0, ends run_end, slots run_w; adjacent and
 // in position order) where the permutation is not consecutive; the cut runs
-// replace them in the same arrays.  Each thread scans 16 positions per pass;
+// replace them in the same arrays.  Each thread scans 32 positions per pass;
 // the break positions are placed by a block scan.  `scratch` is followed by
 // 3 * runcap ints of room.  Returns the new run count (0 and a status bit on
 // overflow).  Every thread of the block calls it.
 static __device__ __noinline__ int split_runs_at_gaps(const LoraParams &p, int runcap, int *run_p0, int *run_end,
-                                               int *run_w, int *scratch, int nruns) {
-    constexpr int PT = 16;
+                                                      int *run_w, int *scratch, int nruns) {
+    constexpr int PT = 32;  // positions per thread per pass, loaded as 16-byte vectors
     int *sub_p0 = scratch + 32, *sub_w = sub_p0 + runcap, *sub_end = sub_w + runcap;
     const int tid = threadIdx.x, nt = blockDim.x;
     const int first = nruns > 0 ? run_p0[0] : 0, last = nruns > 0 ? run_end[nruns - 1] : 0;
     int nsub = 0;
     for (int base = first; base < last; base += nt * PT) {
         const int a = base + tid * PT;
+        int v[PT];
+        if (a + PT <= last && ((a & 3) == 0)) {
+#pragma unroll
+            for (int i = 0; i < PT; i += 4) {
+                const int4 q = *reinterpret_cast<const int4 *>(p.permutation + a + i);
+                v[i] = q.x; v[i + 1] = q.y; v[i + 2] = q.z; v[i + 3] = q.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < PT; ++i) v[i] = a + i < last ? p.permutation[a + i] : 0;
+        }
+        int prev = a > 0 && a < last ? p.permutation[a - 1] : -2;
         int r = 0;  // the run holding position a
         {
             int lo = 0, hi = nruns;
@@ -160,24 +172,23 @@ static __device__ __noinline__ int split_runs_at_gaps(const LoraParams &p, int r
             r = lo;
         }
         uint32_t brk = 0;
-        int prev = a > 0 ? p.permutation[a - 1] : -2;
         int rr = r;
 #pragma unroll
         for (int i = 0; i < PT; ++i) {
             const int pp = a + i;
             if (pp < last) {
                 while (rr + 1 < nruns && run_p0[rr + 1] <= pp) ++rr;
-                const int v = p.permutation[pp];
-                if (pp == run_p0[rr] || v != prev + 1) brk |= 1u << i;
-                prev = v;
+                if (pp == run_p0[rr] || v[i] != prev + 1) brk |= 1u << i;
+                prev = v[i];
             }
         }
         int tot;
         const int pre = block_scan(__popc(brk), scratch, &tot);
         int idx = nsub + pre;
         rr = r;
-        for (int i = 0; i < PT; ++i) {
-            if (!((brk >> i) & 1u)) continue;
+        while (brk) {
+            const int i = __ffs(brk) - 1;
+            brk &= brk - 1;
             const int pp = a + i;
             while (rr + 1 < nruns && run_p0[rr + 1] <= pp) ++rr;
             if (idx < runcap) {

@@ -45,8 +45,9 @@ extern "C" CSGMV_API int csgmv_qkv_static_scratch(const void *x, int64_t K, cons
                                                   csgmv_stream_t stream) {
     if (!bi) return csgmv_qkv(x, K, A, B, N, slice_offsets, num_slices, max_slice_size, base_output, nullptr, 0,
                               bi, stream);  // reports the missing batch info
-    const size_t need = (size_t)(bi->num_tokens > 0 ? bi->num_tokens : 0) * (size_t)(num_slices > 0 ? num_slices : 0) *
-                        (size_t)(bi->max_rank > 0 ? bi->max_rank : 0) * 4;
+    const size_t need = csgmv::kWsHeader + (size_t)(bi->num_tokens > 0 ? bi->num_tokens : 0) *
+                                               (size_t)(num_slices > 0 ? num_slices : 0) *
+                                               (size_t)(bi->max_rank > 0 ? bi->max_rank : 0) * 4;
     if (need > kStaticScratchFloats * 4) {
         char msg[160];
         snprintf(msg, sizeof msg, "csgmv_qkv_static_scratch: h needs %zu bytes, the static scratch holds %zu",
