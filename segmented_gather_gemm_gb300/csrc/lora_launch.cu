@@ -527,8 +527,9 @@ cudaError_t launch_lora_stream(LoraParams &p, const csgmv_batch_info &bi, cudaSt
         ok = ok && encode_2d(&k.tmB[j], p.Bs[jj], (uint64_t)p.R, (uint64_t)L * p.b_rows[jj], (uint64_t)p.R * 2, p.R,
                              64, swizzle_for_row_bytes(p.R * 2));  // one box per 64 columns of a stage
     }
-    ok = ok && encode_2d(&k.tmY, p.y, (uint64_t)p.N, (uint64_t)s, (uint64_t)p.N * 2, 64, 128,
-                         CU_TENSOR_MAP_SWIZZLE_128B);
+    for (int l = 0; l < kRowBoxLevels; ++l)
+        ok = ok && encode_2d(&k.tmY[l], p.y, (uint64_t)p.N, (uint64_t)s, (uint64_t)p.N * 2, 64, 128u >> l,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && encode_2d(&k.tmYs, p.y, (uint64_t)p.N, (uint64_t)s, (uint64_t)p.N * 2, 64, 32,
                          CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && encode_2d(&k.tmYg, p.y, (uint64_t)p.N, (uint64_t)s, (uint64_t)p.N * 2, 64, 1,

@@ -118,11 +118,12 @@ __device__ void st_producer(const StreamParams &k, unsigned char *smem, const in
             mbar_wait(&W.y_empty[sy], ((g / k.Sy) & 1) ^ 1, p.status, kStatusTimeout);
             unsigned char *ys = smem + k.o_yring + sy * k.y_slot_bytes;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&W.y_full[sy], p.accumulate ? kStBoxes * kStTileBytes : 0);
+                mbar_arrive_expect_tx(&W.y_full[sy],
+                                      !p.accumulate ? 0 : contig ? kStBoxes * row_box_bytes(U.M) : kStBoxes * kStTileBytes);
                 if (p.accumulate && contig)
 #pragma unroll
                     for (int bx = 0; bx < kStBoxes; ++bx)
-                        tma_load_2d(ys + bx * kStTileBytes, &k.tmY, x0 + 64 * bx, t0, &W.y_full[sy]);
+                        load_row_boxes(ys + bx * kStTileBytes, k.tmY, x0 + 64 * bx, t0, U.M, &W.y_full[sy]);
             }
             if (p.accumulate && !contig) {
                 // lane l: tile rows 4l .. 4l+3 in one gather per box; rows past the
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(kStThreads, 1) lora_stream_expand_kernel(const
         }
         fence_mbar_init();
         for (int j = 0; j < kMaxSlices; ++j) prefetch_tmap(&k.tmB[j]);
-        prefetch_tmap(&k.tmY);
+        for (int l = 0; l < kRowBoxLevels; ++l) prefetch_tmap(&k.tmY[l]);
         prefetch_tmap(&k.tmYs);
         prefetch_tmap(&k.tmYg);
     }

@@ -62,9 +62,37 @@ constexpr int kStTileBytes = 128 * 128;  // 128 rows x 64 bf16: one base box
 constexpr int kStBSlots = 6;             // B tiles in flight (needed only until their MMAs are done)
 static_assert(kStAcc >= kStTeams, "every team needs an accumulator");
 
+// Base rows of a tile of consecutive tokens move as TMA boxes of 128, 64, 32,
+// 16 and 8 rows (one tensor map each), so that a tile of M < 128 tokens loads
+// round8(M) rows rather than 128.  (The same for the shrink's x rows measured
+// slower: 112 -> 141 us on the prefill shrink.)
+constexpr int kRowBoxLevels = 5;
+
+#ifdef __CUDACC__
+// Rows [0, M) (M <= 128) of the consecutive tokens t0, t0 + 1, ..., columns
+// [x, x + 64), into a 128-byte-swizzled tile of 128-byte rows at dst: M
+// rounded up to 8 as a sum of the box heights, largest first (every box
+// starts on an 8-row, i.e. 1024-byte, boundary).  Returns the bytes loaded.
+__device__ __forceinline__ uint32_t load_row_boxes(void *dst, const CUtensorMap *maps, int x, int t0, int M,
+                                                   uint64_t *bar) {
+    const int Mr = (M + 7) & ~7;
+    int o = 0;
+#pragma unroll
+    for (int l = 0; l < kRowBoxLevels; ++l) {
+        const int h = 128 >> l;
+        if (Mr - o >= h) {
+            tma_load_2d(static_cast<unsigned char *>(dst) + o * 128, &maps[l], x, t0 + o, bar);
+            o += h;
+        }
+    }
+    return (uint32_t)Mr * 128;
+}
+__device__ __forceinline__ uint32_t row_box_bytes(int M) { return (uint32_t)((M + 7) & ~7) * 128; }
+#endif
+
 struct StreamParams {
     CUtensorMap tmB[kMaxSlices];  // slice j of B: L * b_rows[j] rows of R bf16, box R x 64
-    CUtensorMap tmY;              // base / y (s rows, N): box 64 x 128, 128-byte swizzle (loads)
+    CUtensorMap tmY[kRowBoxLevels];  // base / y (s rows, N): boxes 64 x (128 >> l), 128-byte swizzle (loads)
     CUtensorMap tmYs;             // the same, box 64 x 32 (one epilogue warp's store)
     CUtensorMap tmYg;             // the same, box 64 x 1 (4-row gathers)
     LoraParams p;
