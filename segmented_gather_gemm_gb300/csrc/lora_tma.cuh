@@ -137,69 +137,92 @@ __device__ __forceinline__ int block_scan(int v, int *scratch, int *total) {
 
 // Cuts the slot runs (starts run_p0, ends run_end, slots run_w; adjacent and
 // in position order) where the permutation is not consecutive; the cut runs
-// replace them in the same arrays.  Each thread scans 32 positions per pass;
-// the break positions are placed by a block scan.  `scratch` is followed by
-// 3 * runcap ints of room.  Returns the new run count (0 and a status bit on
-// overflow).  Every thread of the block calls it.
+// replace them in the same arrays.  Within a slot run the stable sort keeps
+// tokens in increasing order, so g(p) = permutation[p] - p never decreases
+// there: a stretch of one run holds a gap exactly when g differs at its two
+// ends, and each gap is found by a binary search.  Each thread takes one
+// stretch of about s / threads positions; a stretch with more than kMaxGaps
+// cuts is scanned position by position instead.  A gap this misses (an
+// out-of-range entry breaks the order) only costs speed: every tile's rows
+// are checked for consecutiveness before they are loaded as a box.
+// `scratch` is followed by 3 * runcap ints of room.  Returns the new run
+// count (0 and a status bit on overflow).  Every thread of the block calls it.
 static __device__ __noinline__ int split_runs_at_gaps(const LoraParams &p, int runcap, int *run_p0, int *run_end,
                                                       int *run_w, int *scratch, int nruns) {
-    constexpr int PT = 32;  // positions per thread per pass, loaded as 16-byte vectors
+    constexpr int kMaxGaps = 8;
     int *sub_p0 = scratch + 32, *sub_w = sub_p0 + runcap, *sub_end = sub_w + runcap;
     const int tid = threadIdx.x, nt = blockDim.x;
     const int first = nruns > 0 ? run_p0[0] : 0, last = nruns > 0 ? run_end[nruns - 1] : 0;
-    int nsub = 0;
-    for (int base = first; base < last; base += nt * PT) {
-        const int a = base + tid * PT;
-        int v[PT];
-        if (a + PT <= last && ((a & 3) == 0)) {
-#pragma unroll
-            for (int i = 0; i < PT; i += 4) {
-                const int4 q = *reinterpret_cast<const int4 *>(p.permutation + a + i);
-                v[i] = q.x; v[i + 1] = q.y; v[i + 2] = q.z; v[i + 3] = q.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < PT; ++i) v[i] = a + i < last ? p.permutation[a + i] : 0;
+    const int stretch = max(1, (last - first + nt - 1) / nt);
+    const int a = min(last, first + tid * stretch), b = min(last, a + stretch);
+    auto g = [&](int pp) { return p.permutation[pp] - pp; };
+    int r0 = 0;  // the run holding position a
+    {
+        int lo = 0, hi = nruns;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (run_p0[mid] <= a) lo = mid; else hi = mid;
         }
-        int prev = a > 0 && a < last ? p.permutation[a - 1] : -2;
-        int r = 0;  // the run holding position a
-        {
-            int lo = 0, hi = nruns;
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (run_p0[mid] <= a) lo = mid; else hi = mid;
-            }
-            r = lo;
-        }
-        uint32_t brk = 0;
-        int rr = r;
-#pragma unroll
-        for (int i = 0; i < PT; ++i) {
-            const int pp = a + i;
-            if (pp < last) {
-                while (rr + 1 < nruns && run_p0[rr + 1] <= pp) ++rr;
-                if (pp == run_p0[rr] || v[i] != prev + 1) brk |= 1u << i;
-                prev = v[i];
-            }
-        }
-        int tot;
-        const int pre = block_scan(__popc(brk), scratch, &tot);
-        int idx = nsub + pre;
-        rr = r;
-        while (brk) {
-            const int i = __ffs(brk) - 1;
-            brk &= brk - 1;
-            const int pp = a + i;
-            while (rr + 1 < nruns && run_p0[rr + 1] <= pp) ++rr;
-            if (idx < runcap) {
-                sub_p0[idx] = pp;
-                sub_w[idx] = run_w[rr];
-                sub_end[idx] = run_end[rr];
-            }
-            ++idx;
-        }
-        nsub += tot;
+        r0 = lo;
     }
+    // cut at x (a <= x < last): a run starts there, or x - 1 (same run) is not its predecessor token
+    auto cut_at = [&](int x, int r) { return x == run_p0[r] || p.permutation[x] != p.permutation[x - 1] + 1; };
+    int cuts[kMaxGaps];
+    int nc = 0;
+    bool linear = false;
+    for (int u = a, r = r0; u < b && !linear; ++r) {
+        const int v = min(b, run_end[r]);  // piece [u, v) of run r
+        if (cut_at(u, r)) {
+            if (nc == kMaxGaps) { linear = true; break; }
+            cuts[nc++] = u;
+        }
+        int lo = u;
+        const int gv = g(v - 1);
+        while (lo < v - 1 && g(lo) != gv) {
+            const int gl = g(lo);
+            int L = lo + 1, H = v - 1;  // first x in (lo, v) with g(x) > g(lo)
+            while (L < H) {
+                const int M = (L + H) >> 1;
+                if (g(M) > gl) H = M; else L = M + 1;
+            }
+            if (nc == kMaxGaps) { linear = true; break; }
+            cuts[nc++] = L;
+            lo = L;
+        }
+        u = v;
+    }
+    int count = nc;
+    if (linear) {
+        count = 0;
+        for (int x = a, r = r0; x < b; ++x) {
+            while (r + 1 < nruns && run_p0[r + 1] <= x) ++r;
+            count += cut_at(x, r);
+        }
+    }
+    int tot;
+    const int pre = block_scan(count, scratch, &tot);
+    int idx = pre;
+    auto put = [&](int x, int r) {
+        if (idx < runcap) {
+            sub_p0[idx] = x;
+            sub_w[idx] = run_w[r];
+            sub_end[idx] = run_end[r];
+        }
+        ++idx;
+    };
+    if (linear) {
+        for (int x = a, r = r0; x < b; ++x) {
+            while (r + 1 < nruns && run_p0[r + 1] <= x) ++r;
+            if (cut_at(x, r)) put(x, r);
+        }
+    } else {
+        int r = r0;
+        for (int i = 0; i < nc; ++i) {
+            while (r + 1 < nruns && run_p0[r + 1] <= cuts[i]) ++r;
+            put(cuts[i], r);
+        }
+    }
+    int nsub = tot;
     if (nsub > runcap) {
         if (tid == 0) atomicOr(p.status, CSGMV_STATUS_CAPACITY);
         nsub = 0;
