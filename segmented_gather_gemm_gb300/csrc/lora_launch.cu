@@ -479,7 +479,8 @@ cudaError_t launch_lora_sshrink(LoraParams &p, const csgmv_batch_info &bi, cudaS
 
 // Expand-only calls on 128-token tiles: the streaming tcgen05 kernel, one CTA
 // per SM.  Units are (tile, column block inside one slice); the column block
-// is sized so that every CTA gets about sixteen units.
+// is sized so that every CTA gets about sixteen units, and holds at least
+// 16 R columns.
 cudaError_t launch_lora_stream(LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream, LaunchInfo *info) {
     const void *fn = lora_kernel_stream();
     cudaError_t e = encoder();  // the tensor-map encoder, resolved on first use
@@ -508,11 +509,15 @@ cudaError_t launch_lora_stream(LoraParams &p, const csgmv_batch_info &bi, cudaSt
 
     const int s = p.num_tokens;
     const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
-    const int tiles_est = (s + 127) / 128 + slots / 2;
-    const int tiles_ub = (s + 127) / 128 + std::min(std::max(bi.bs, 1), std::max(bi.max_loras, 1));
+    // tiles are cut at slot runs and at request boundaries: about half a
+    // partial tile for each
+    const int tiles_est = (s + 127) / 128 + (slots + std::max(bi.bs, 1)) / 2;
+    const int tiles_ub = (s + 127) / 128 + std::max(bi.bs, 1) + std::min(std::max(bi.bs, 1), std::max(bi.max_loras, 1));
     const int64_t ncols = p.off[p.c] - p.off[0];
+    // at least 16 R columns: each unit reads h of its tile once (up to four
+    // partial-sum planes of 128 x R floats), small next to its base rows
     int64_t cb = (int64_t)tiles_est * ncols / ((int64_t)16 * res);
-    cb = std::max<int64_t>(512, (cb + 63) / 64 * 64);
+    cb = std::max<int64_t>(std::max(512, 16 * p.R), (cb + 63) / 64 * 64);
     k.cb = (int)std::min<int64_t>(cb, 1 << 30);
     k.upt = 0;
     for (int j = 0; j < p.c; ++j) k.upt += (p.off[j + 1] - p.off[j] + k.cb - 1) / k.cb;
