@@ -110,20 +110,33 @@ def algorithmic(w, chunk: int) -> dict:
 
 
 WIDE_COLS = 32768  # the library's kWideCols
+DECODE_CAPS = {"segments": 512, "loras": 256, "tokens": 2048}  # the decode kernels' table capacities
 
 
 def qkv_kernels(w, bi) -> int:
     """Kernels one csgmv_qkv call launches when given a workspace: two (shrink,
     expand) where the library takes its two-kernel path, else one.  The path
-    is taken by 16- / 32-token tiles with at least WIDE_COLS output columns,
-    and by 128-token tiles with a buffer rank R >= 16.  Mirrors the library's
-    choice for the gpu_launches count."""
+    is taken by 16- / 32-token tiles (the decode kernels when the batch info's
+    capacities fit their tables, the small-tile kernel with at least WIDE_COLS
+    output columns) and by 128-token tiles with a buffer rank R >= 16.
+    With a built batch info `bi` this is the library's own answer
+    (csgmv_qkv_path with csgmv_qkv_workspace_bytes of workspace); without one
+    the rule is applied here with the bench's capacities (max_segments =
+    tokens + 1), which a host test checks against the library."""
     if isinstance(w, wl.EmbeddingWorkload):
         return 1
+    if bi is not None and bi.c.num_tokens >= 0:
+        from segmented_gather_gemm_gb300 import binding as B
+        ws = B.csgmv_qkv_workspace_bytes(bi, w.c)
+        return 1 if B.csgmv_qkv_path(bi, w.K, w.N, w.offsets, w.c, ws) == "fused" else 2
     slots = max(1, min(max(w.bs, 1), w.L))
     tm = 16 if w.s // slots <= 16 else (32 if w.s // slots <= 48 else 128)
     if tm <= 32:
-        split = int(w.offsets[-1]) - int(w.offsets[0]) >= WIDE_COLS
+        max_segments = bi.c.max_segments if bi is not None else w.s + 1
+        max_loras = bi.c.max_loras if bi is not None else w.L
+        decode = (max_segments <= DECODE_CAPS["segments"] and max_loras <= DECODE_CAPS["loras"]
+                  and w.s <= DECODE_CAPS["tokens"])
+        split = int(w.offsets[-1]) - int(w.offsets[0]) >= WIDE_COLS or decode
     else:
         split = w.R >= 16
     return 2 if split else 1
@@ -149,7 +162,7 @@ def load_peaks():
 # shapes, the warp-specialized shrink and the tcgen05 expand for prefill.
 _SHARED_SOURCES = ("lora_tma.cuh", "lora_launch.cu", "device_utils.cuh", "csgmv_internal.h")
 KERNEL_SOURCES = {
-    "decode_qkv": ("lora_small.cuh", "lora_small.cu") + _SHARED_SOURCES,
+    "decode_qkv": ("lora_decode.cuh", "lora_decode.cu") + _SHARED_SOURCES,
     "lm_head_decode": ("lora_small.cuh", "lora_small.cu") + _SHARED_SOURCES,
     "prefill_gate_up": ("lora_stream.cuh", "lora_stream.cu", "lora_sshrink.cu") + _SHARED_SOURCES,
     "skewed_down_proj": ("lora_stream.cuh", "lora_stream.cu", "lora_sshrink.cu") + _SHARED_SOURCES,

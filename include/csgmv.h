@@ -97,7 +97,21 @@ typedef struct csgmv_batch_info {
     int32_t max_segments, max_tokens, max_loras, max_bs, max_rank;
     /* host mirror of the current batch (set by csgmv_build_batch_info) */
     int32_t num_tokens, chunk_size, bs, num_loras, use_cuda_graph;
+    /* Optional (NULL for none): the token tiles of the current batch, for the
+     * decode kernels of csgmv_qkv, so that no CTA rebuilds them from the
+     * segments.  csgmv_build_batch_info writes [0] = tile count and [1..3] =
+     * 0, then per tile {slot, first sorted position, tokens, 0}: every slot
+     * run (a maximal stretch of segments on one slot) cut into
+     * ceil(n / 64) tiles of balanced size, in segment order;
+     * csgmv_build_lm_head_batch_info writes [0] = -1 (no tiles: the kernels
+     * derive them from the segments).  csgmv_tile_table_ints() gives its
+     * int32 length. */
+    int32_t *tile_table;
 } csgmv_batch_info;
+
+/* int32 entries of csgmv_batch_info.tile_table for these capacities:
+ * 4 * (max_loras + max_tokens / 64 + 2).  Host only; 0 for negative sizes. */
+CSGMV_API int64_t csgmv_tile_table_ints(int max_loras, int max_tokens);
 
 /* Message of the last failed call on this thread ("" if none). */
 CSGMV_API const char *csgmv_last_error(void);
@@ -223,10 +237,14 @@ CSGMV_API int csgmv_expand(const void *h, int h_dtype, int64_t ldh, const void *
  *       max_rank * 4 bytes; csgmv_qkv_workspace_bytes() covers every batch
  *       and the widest split of K), two kinds of call instead run the shrink and the expand
  *       as two kernels with h in the workspace, which is faster there:
- *       batches of long per-slot runs (128-token tiles, max_rank >= 16; the
- *       shrink may cut K into parts, one plane of partial sums each, that the
- *       expand adds in order), and short per-slot runs with at least 32768
- *       output columns (a vocabulary-wide lm_head).  Its contents on entry do
+ *       batches of long per-slot runs (128-token tiles, max_rank >= 16),
+ *       decode batches (short per-slot runs onto fewer than 32768 columns,
+ *       at most 2048 tokens, max_segments <= 512 and max_loras <= 256), and
+ *       short per-slot runs with at least 32768 output columns (a
+ *       vocabulary-wide lm_head).  The shrink may cut K into parts, one plane
+ *       of partial sums each, that the expand adds in part order, so results
+ *       do not depend on timing.  csgmv_qkv_path() tells which path a call
+ *       takes.  Its contents on entry do
  *       not matter; on return they are unspecified.  It must be 16-byte
  *       aligned and must not overlap any other argument.
  */
@@ -254,11 +272,34 @@ CSGMV_API int csgmv_qkv_sliced(const void *x, int64_t K, const void *A, const vo
                                void *workspace, size_t workspace_bytes, const csgmv_batch_info *bi,
                                csgmv_stream_t stream);
 
-/* Workspace bytes that let csgmv_qkv use its two-kernel path for any batch
- * of this batch info, with h (fp32) held as up to four partial sums over parts
- * of K after a 256-byte header: 256 + 4 * max_tokens * num_slices * max_rank
- * * 4.  A smaller workspace of at least 256 + num_tokens * num_slices *
- * max_rank * 4 bytes also takes the path, with fewer parts. */
+/* Kernel paths of csgmv_qkv (csgmv_qkv_path). */
+enum {
+    CSGMV_PATH_FUSED = 0,       /* one kernel: h reduced across a thread-block cluster, never in memory */
+    CSGMV_PATH_DECODE = 1,      /* decode batches: split-K shrink into fp32 planes, then the expand */
+    CSGMV_PATH_SMALL_SPLIT = 2, /* short runs onto vocabulary-wide outputs: small-tile shrink, then expand */
+    CSGMV_PATH_STREAM = 3       /* 128-token tiles: streaming tcgen05 shrink, then streaming expand */
+};
+
+/*
+ * The path csgmv_qkv takes for the batch last built into bi, with these
+ * shapes (as csgmv_qkv's K, N, slice_offsets, num_slices) and a workspace of
+ * workspace_bytes (0 for none).  Host only: reads the capacity and host
+ * mirror fields of bi, launches nothing, needs no GPU.  Returns a
+ * CSGMV_PATH_* value (CSGMV_PATH_FUSED for an empty batch), or
+ * CSGMV_ERR_INVALID_ARG / CSGMV_ERR_UNSUPPORTED as csgmv_qkv would for the
+ * same shapes.  Paths other than CSGMV_PATH_FUSED launch two kernels.
+ */
+CSGMV_API int csgmv_qkv_path(const csgmv_batch_info *bi, int64_t K, int64_t N, const int32_t *slice_offsets,
+                             int num_slices, size_t workspace_bytes);
+
+/* Workspace bytes that let csgmv_qkv use its two-kernel paths for any batch
+ * of this batch info, with h (fp32) held as partial sums over parts of K
+ * (planes of max_tokens * num_slices * max_rank floats) after a 256-byte
+ * header: 256 + P * max_tokens * num_slices * max_rank * 4 with P = 4, or
+ * P = 32 * min(max_tokens, 2048) / max_tokens when that is more (room for the
+ * decode kernels' 32 parts).  A smaller workspace of at least 256 +
+ * num_tokens * num_slices * max_rank * 4 bytes also takes the paths, with
+ * fewer parts. */
 CSGMV_API size_t csgmv_qkv_workspace_bytes(const csgmv_batch_info *bi, int num_slices);
 
 /*

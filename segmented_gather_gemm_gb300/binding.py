@@ -24,7 +24,10 @@ STATUS_BITS = {
 EXPORTED = ["csgmv_last_error", "csgmv_version", "csgmv_chunk_size", "csgmv_batch_info_capacity",
             "csgmv_build_batch_info", "csgmv_build_lm_head_batch_info", "csgmv_shrink", "csgmv_expand", "csgmv_qkv", "csgmv_qkv_workspace_bytes",
             "csgmv_qkv_static_scratch", "embedding_lora_a", "embedding_lora_a_extra", "extra_token_embedding",
-            "csgmv_expand_sliced", "csgmv_qkv_sliced"]
+            "csgmv_expand_sliced", "csgmv_qkv_sliced", "csgmv_qkv_path", "csgmv_tile_table_ints"]
+
+# csgmv_qkv_path results (CSGMV_PATH_*)
+PATHS = {0: "fused", 1: "decode", 2: "small_split", 3: "stream"}
 
 
 class CsgmvError(RuntimeError):
@@ -39,7 +42,8 @@ class _BatchInfoC(ctypes.Structure):
         "max_len_dev", "req_seg_indptr", "req_weight_indices", "status")] + [
         (n, ctypes.c_int32) for n in (
             "max_segments", "max_tokens", "max_loras", "max_bs", "max_rank",
-            "num_tokens", "chunk_size", "bs", "num_loras", "use_cuda_graph")]
+            "num_tokens", "chunk_size", "bs", "num_loras", "use_cuda_graph")] + [
+        ("tile_table", ctypes.c_void_p)]
 
 
 _lib = None
@@ -75,6 +79,8 @@ def lib():
         "csgmv_qkv_sliced": (i32, [vp, i64, vp, ctypes.POINTER(vp), i64, i32p, i32, i32, vp, vp, ctypes.c_size_t,
                                    bip, vp]),
         "extra_token_embedding": (i32, [vp, vp, i64, vp, i64, i64, bip, vp]),
+        "csgmv_qkv_path": (i32, [bip, i64, i64, i32p, i32, ctypes.c_size_t]),
+        "csgmv_tile_table_ints": (i64, [i32, i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -118,12 +124,21 @@ def csgmv_batch_info_capacity(max_bs: int, num_tokens_per_bs: int) -> tuple[int,
     return int(ms.value), int(mt.value)
 
 
+def tile_table_ints(max_loras: int, max_tokens: int) -> int:
+    """int32 entries of a batch info's tile table (csgmv_tile_table_ints)."""
+    return 4 * (max(max_loras, 0) + max(max_tokens, 0) // 64 + 2)
+
+
+def csgmv_tile_table_ints(max_loras: int, max_tokens: int) -> int:
+    return int(lib().csgmv_tile_table_ints(int(max_loras), int(max_tokens)))
+
+
 class BatchInfo:
     """Device buffers of one batch info (caller-owned, allocated once by torch)
     plus the C struct that points at them."""
 
     def __init__(self, max_bs: int, max_tokens: int, max_segments: int, max_loras: int, max_rank: int,
-                 device="cuda", with_request_fields: bool = True):
+                 device="cuda", with_request_fields: bool = True, with_tile_table: bool = True):
         dev = torch.device(device)
         i32 = dict(dtype=torch.int32, device=dev)
         self.seg_indptr = torch.zeros(max_segments + 1, **i32)
@@ -136,9 +151,10 @@ class BatchInfo:
         self.status = torch.zeros(1, **i32)
         self.req_seg_indptr = torch.zeros(max_bs + 1, **i32) if with_request_fields else None
         self.req_weight_indices = torch.zeros(max(max_bs, 1), **i32) if with_request_fields else None
+        self.tile_table = torch.zeros(tile_table_ints(max_loras, max_tokens), **i32) if with_tile_table else None
         c = _BatchInfoC()
         for n in ("seg_indptr", "weight_indices", "permutation", "lora_ranks", "scalings", "status",
-                  "req_seg_indptr", "req_weight_indices"):
+                  "req_seg_indptr", "req_weight_indices", "tile_table"):
             t = getattr(self, n)
             setattr(c, n, t.data_ptr() if t is not None else None)
         c.num_segments_dev = self.num_segments.data_ptr()
@@ -225,6 +241,17 @@ def csgmv_qkv(x: torch.Tensor, A: torch.Tensor, B: torch.Tensor, slice_offsets, 
     _check(lib().csgmv_qkv(_ptr(x), K, _ptr(A), _ptr(B), N, _offsets(slice_offsets), int(num_slices),
                            int(max_slice_size), _ptr(base_output), ws, wsb, ctypes.byref(bi.c), _stream(stream)))
     return base_output
+
+
+def csgmv_qkv_path(bi: BatchInfo, K: int, N: int, slice_offsets, num_slices: int, workspace_bytes: int) -> str:
+    """Which kernels csgmv_qkv runs for the batch last built into bi: "fused"
+    (one kernel) or a two-kernel path ("decode", "small_split", "stream").
+    Host only."""
+    rc = lib().csgmv_qkv_path(ctypes.byref(bi.c), int(K), int(N), _offsets(slice_offsets), int(num_slices),
+                              int(workspace_bytes))
+    if rc < 0:
+        _check(rc)
+    return PATHS[rc]
 
 
 def csgmv_qkv_workspace_bytes(bi: BatchInfo, num_slices: int) -> int:

@@ -56,7 +56,9 @@ bool overlaps_batch_info(const csgmv_batch_info *bi, const void *out, size_t byt
            overlaps(out, bytes, bi->lora_ranks, 4 * (size_t)bi->max_loras) ||
            overlaps(out, bytes, bi->scalings, 4 * (size_t)bi->max_loras) ||
            overlaps(out, bytes, bi->num_segments_dev, 4) || overlaps(out, bytes, bi->max_len_dev, 4) ||
-           overlaps(out, bytes, bi->status, 4);
+           overlaps(out, bytes, bi->status, 4) ||
+           (bi->tile_table &&
+            overlaps(out, bytes, bi->tile_table, 4 * (size_t)csgmv_tile_table_ints(bi->max_loras, bi->max_tokens)));
 }
 
 int check_bi(const csgmv_batch_info *bi, bool built) {
@@ -120,6 +122,7 @@ void fill_common(csgmv::LoraParams &p, const csgmv_batch_info *bi) {
     p.scalings = bi->scalings;
     p.num_segments_dev = bi->num_segments_dev;
     p.max_len_dev = bi->max_len_dev;
+    p.tile_table = bi->tile_table;
     p.status = bi->status;
     p.num_tokens = bi->num_tokens;
     p.max_loras = bi->max_loras;
@@ -224,9 +227,11 @@ int qkv_impl(const void *x, int64_t K, const void *A, const void *B, const void 
     set_b(p, B_slices);
     p.accumulate = 1;
     const size_t hbytes = (size_t)s * num_slices * bi->max_rank * 4;
-    if (workspace && workspace_bytes >= csgmv::kWsHeader + hbytes && csgmv::qkv_split_pays(p, *bi)) {
-        // the header and the planes of h the call may write: up to kMaxKParts of hbytes
-        const size_t ws_used = std::min(workspace_bytes, csgmv::kWsHeader + (size_t)csgmv::kMaxKParts * hbytes);
+    const int path = csgmv::qkv_path(p, *bi, workspace ? workspace_bytes : 0);
+    if (path != CSGMV_PATH_FUSED) {
+        // the header and the planes of h the call may write (parts of K, hbytes each)
+        const size_t ws_used =
+            std::min(workspace_bytes, csgmv::kWsHeader + (size_t)csgmv::qkv_max_parts(p, *bi) * hbytes);
         if (!aligned16(workspace)) return fail(CSGMV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
         if (overlaps_batch_info(bi, workspace, ws_used) ||
             overlaps(workspace, ws_used, base_output, (size_t)s * N * 2))
@@ -249,7 +254,7 @@ int qkv_impl(const void *x, int64_t K, const void *A, const void *B, const void 
         pe.h_f32 = 1;
         pe.ldh = ps.ldh;
         cudaError_t e =
-            csgmv::launch_qkv_split(ps, pe, *bi, reinterpret_cast<cudaStream_t>(stream), workspace, ws_used);
+            csgmv::launch_qkv_split(ps, pe, *bi, reinterpret_cast<cudaStream_t>(stream), workspace, ws_used, path);
         if (e != cudaSuccess) return cuda_fail(e, "csgmv_qkv shrink / expand launch");
         return CSGMV_OK;
     }
@@ -413,9 +418,40 @@ int csgmv_expand_sliced(const void *h, int h_dtype, int64_t ldh, const void *con
                        accumulate, bi, stream);
 }
 
+int64_t csgmv_tile_table_ints(int max_loras, int max_tokens) {
+    if (max_loras < 0 || max_tokens < 0) return 0;
+    return 4 * ((int64_t)max_loras + max_tokens / csgmv::kDecTM + 2);
+}
+
+int csgmv_qkv_path(const csgmv_batch_info *bi, int64_t K, int64_t N, const int32_t *slice_offsets, int num_slices,
+                   size_t workspace_bytes) {
+    int rc = check_bi(bi, true);
+    if (rc) return rc;
+    if ((rc = check_rank(bi))) return rc;
+    int widest = 0;
+    if (slice_offsets && num_slices >= 1 && num_slices <= csgmv::kMaxSlices)
+        for (int j = 0; j < num_slices; ++j) widest = std::max(widest, slice_offsets[j + 1] - slice_offsets[j]);
+    if ((rc = check_offsets(slice_offsets, num_slices, N, widest))) return rc;
+    if (K <= 0 || K % 8 != 0 || K > INT32_MAX) return fail(CSGMV_ERR_INVALID_ARG, "K %lld must be a positive multiple of 8", (long long)K);
+    if (N <= 0 || N % 8 != 0 || N > INT32_MAX) return fail(CSGMV_ERR_INVALID_ARG, "N %lld must be a positive multiple of 8", (long long)N);
+    csgmv::LoraParams p = {};
+    fill_common(p, bi);
+    p.K = K;
+    p.N = N;
+    p.c = num_slices;
+    for (int j = 0; j <= num_slices; ++j) p.off[j] = slice_offsets[j];
+    p.accumulate = 1;
+    return csgmv::qkv_path(p, *bi, workspace_bytes);
+}
+
 size_t csgmv_qkv_workspace_bytes(const csgmv_batch_info *bi, int num_slices) {
     if (!bi || bi->max_tokens < 0 || bi->max_rank < 0 || num_slices < 1 || num_slices > csgmv::kMaxSlices) return 0;
-    return csgmv::kWsHeader + (size_t)csgmv::kMaxKParts * bi->max_tokens * num_slices * bi->max_rank * 4;
+    // up to kMaxKParts planes of every token, or kDecMaxParts planes of a
+    // batch small enough for the decode kernels
+    const size_t T = (size_t)bi->max_tokens;
+    const size_t rows = std::max((size_t)csgmv::kMaxKParts * T,
+                                 (size_t)csgmv::kDecMaxParts * std::min(T, (size_t)csgmv::kDecPermCap));
+    return csgmv::kWsHeader + rows * num_slices * bi->max_rank * 4;
 }
 
 int csgmv_qkv(const void *x, int64_t K, const void *A, const void *B, int64_t N, const int32_t *slice_offsets,

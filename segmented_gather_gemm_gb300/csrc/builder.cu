@@ -189,6 +189,7 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
             *bi.num_segments_dev = 0;
             *bi.max_len_dev = chunk;
             bi.seg_indptr[0] = 0;
+            if (bi.tile_table) bi.tile_table[0] = 0;
             *bi.status = err;
         }
         return;
@@ -266,6 +267,37 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
     for (int t = tid; t < p.num_tokens; t += kBuildThreads) {
         int i = last_not_greater(req_start, p.bs + 1, t);
         bi.permutation[req_dest[i] + (t - req_start[i])] = t;
+    }
+
+    // Decode tiles (csgmv_batch_info.tile_table): slots in ascending order are
+    // the slot runs; slot a's cnt[a] tokens become ceil(cnt[a] / kDecTM)
+    // tiles of balanced size.  The running positions in run[] are no longer
+    // needed: it takes the first tile of each slot.
+    if (bi.tile_table) {
+        __syncthreads();  // every thread is past its last use of run[]
+        int tcarry = 0;
+        for (int a0 = 0; a0 < L; a0 += kBuildThreads) {
+            const int a = a0 + tid;
+            const int nt = a < L ? (cnt[a] + kDecTM - 1) / kDecTM : 0;
+            int tot;
+            const int pre = block_exclusive_scan(nt, warp_sums, &tot);
+            if (a < L) run[a] = tcarry + pre;
+            tcarry += tot;
+        }
+        __syncthreads();
+        int *rec = bi.tile_table + 4;
+        for (int t = tid; t < tcarry; t += kBuildThreads) {
+            const int a = last_not_greater(run, L, t);  // the last slot whose tiles start at or before t
+            const int n = cnt[a];
+            const int nt = (n + kDecTM - 1) / kDecTM;
+            const int i = t - run[a];
+            const int lo = i * n / nt, hi = (i + 1) * n / nt;
+            rec[4 * t] = a;
+            rec[4 * t + 1] = tokbase[a] + lo;
+            rec[4 * t + 2] = hi - lo;
+            rec[4 * t + 3] = 0;
+        }
+        if (tid < 4) bi.tile_table[tid] = tid == 0 ? tcarry : 0;
     }
 
     // Per-request fields (chunked_backend.py _build_req_seg_indptr, req_weight_indices).
@@ -362,6 +394,8 @@ build_lm_head_kernel(BuildParams p, csgmv_batch_info bi) {
     }
     __syncthreads();
     const int err = flags[0];
+    // no tile table: the decode kernels derive tiles from the segments
+    if (tid == 0 && bi.tile_table) bi.tile_table[0] = -1;
     if (err) {
         if (tid == 0) {
             *bi.num_segments_dev = 0;

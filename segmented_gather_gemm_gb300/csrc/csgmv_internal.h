@@ -13,6 +13,9 @@ constexpr int kMaxSlices = 3;
 constexpr int kWideCols = 32768;   // output columns from which 16- / 32-token csgmv_qkv calls split
 constexpr int kMaxKParts = 4;      // fp32 h planes of the csgmv_qkv workspace (parts of K)
 constexpr size_t kWsHeader = 256;  // bytes before the planes: the part count the shrink chose
+constexpr int kDecMaxParts = 32;   // planes of the decode kernels' split-K shrink
+constexpr int kDecTM = 64;         // tokens of one decode tile at most (the batch info's tile table)
+constexpr int kDecPermCap = 2048;  // tokens of a batch the decode kernels take
 
 #ifdef __CUDACC__
 // Programmatic dependent launch.  A kernel launched with
@@ -61,6 +64,7 @@ struct LoraParams {
     const int32_t *seg_indptr, *weight_indices, *permutation, *lora_ranks;
     const float *scalings;
     const int32_t *num_segments_dev, *max_len_dev;
+    const int32_t *tile_table;  // the batch info's decode tiles, or NULL
     int32_t *status;
     // shared-memory carve-up (bytes from the dynamic base), chosen on the host
     int sm_tok, sm_stage, sm_hpart, sm_hred, sm_hbf, sm_ex;
@@ -86,12 +90,18 @@ int set_error(int code, const char *msg);
 
 // Whether csgmv_qkv should run as shrink + expand through a workspace.
 bool qkv_split_pays(const LoraParams &p, const csgmv_batch_info &bi);
-// csgmv_qkv's two-kernel path: shrink (ps) into the fp32 workspace (a
+// Planes of h (parts of K) that path may write: kMaxKParts, or kDecMaxParts
+// for the decode kernels.
+int qkv_max_parts(const LoraParams &p, const csgmv_batch_info &bi);
+// The CSGMV_PATH_* csgmv_qkv takes for p (accumulating, as csgmv_qkv) with a
+// workspace of workspace_bytes (0 for none).
+int qkv_path(const LoraParams &p, const csgmv_batch_info &bi, size_t workspace_bytes);
+// csgmv_qkv's two-kernel paths: shrink (ps) into the fp32 workspace (a
 // kWsHeader-byte header, then up to (workspace_bytes - kWsHeader) /
 // (s * c * R * 4) partial-sum planes over parts of K), then the expand (pe)
-// from it.
+// from it, on the kernels of `path` (a two-kernel CSGMV_PATH_*).
 cudaError_t launch_qkv_split(LoraParams &ps, LoraParams &pe, const csgmv_batch_info &bi, cudaStream_t stream,
-                             void *workspace, size_t workspace_bytes);
+                             void *workspace, size_t workspace_bytes, int path);
 
 // builder.cu
 struct BuildParams {

@@ -7,6 +7,7 @@
 #include <mutex>
 #include <tuple>
 
+#include "lora_decode.cuh"
 #include "lora_small.cuh"
 #include "lora_stream.cuh"
 
@@ -18,6 +19,7 @@ const void *lora_kernel_expand(int tm, int rmax, bool tc);
 const void *lora_kernel_small(int mode, int tm, int rmax);
 const void *lora_kernel_stream();
 const void *lora_kernel_sshrink();
+const void *lora_kernel_decode(int which, int rmax);
 
 namespace {
 
@@ -62,30 +64,35 @@ CUtensorMapSwizzle swizzle_for_row_bytes(int bytes) {
 // B of the expand: one (L, N, R) tensor in tmB (box R x box_rows), or, with
 // separate slice tensors, slice j in tmBs[j] (box R x 64); unused maps are
 // copies of a valid one.
-bool encode_b(TmaKernelParams &k, int L, uint32_t box_rows) {
-    const LoraParams &p = k.p;
+bool encode_b_maps(CUtensorMap *tmB, CUtensorMap *tmBs, const LoraParams &p, int L, uint32_t box_rows) {
     const CUtensorMapSwizzle sw = swizzle_for_row_bytes(p.R * 2);
     if (!p.b_tuple) {
-        if (!encode_2d(&k.tmB, p.B, (uint64_t)p.R, (uint64_t)L * p.N, (uint64_t)p.R * 2, p.R, box_rows, sw))
+        if (!encode_2d(tmB, p.B, (uint64_t)p.R, (uint64_t)L * p.N, (uint64_t)p.R * 2, p.R, box_rows, sw))
             return false;
-        for (int j = 0; j < kMaxSlices; ++j) k.tmBs[j] = k.tmB;
+        for (int j = 0; j < kMaxSlices; ++j) tmBs[j] = *tmB;
         return true;
     }
     for (int j = 0; j < kMaxSlices; ++j) {
         const int jj = j < p.c ? j : 0;
-        if (!encode_2d(&k.tmBs[j], p.Bs[jj], (uint64_t)p.R, (uint64_t)L * p.b_rows[jj], (uint64_t)p.R * 2, p.R, 64,
+        if (!encode_2d(&tmBs[j], p.Bs[jj], (uint64_t)p.R, (uint64_t)L * p.b_rows[jj], (uint64_t)p.R * 2, p.R, 64,
                        sw))
             return false;
     }
-    k.tmB = k.tmBs[0];
+    *tmB = tmBs[0];
     return true;
 }
+bool encode_b(TmaKernelParams &k, int L, uint32_t box_rows) { return encode_b_maps(&k.tmB, k.tmBs, k.p, L, box_rows); }
 
 cudaError_t ensure_attrs(const void *fn, int dev, int cluster) {
     std::lock_guard<std::mutex> lk(g_mu);
     auto key = std::make_pair(fn, dev);
     if (g_attr.count(key)) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    // the whole unified L1 as shared memory: an SM configured for one kernel
+    // then also takes the CTAs of a dependent kernel launched behind it
+    // without first draining to change its carve-out
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     (void)cluster;  // clusters of up to 16 CTAs
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -571,19 +578,141 @@ int token_tile(const LoraParams &p, const csgmv_batch_info &bi) {
     return tps <= 16 ? 16 : (tps <= 48 ? 32 : 128);
 }
 
+// Decode-shaped batches the cluster-free decode kernels take: short slot
+// runs, outputs narrower than a vocabulary, and batch-info capacities within
+// the kernels' one-round tables.
+bool decode_fits(const LoraParams &p, const csgmv_batch_info &bi) {
+    return token_tile(p, bi) <= 32 && p.off[p.c] - p.off[0] < kWideCols && p.accumulate &&
+           bi.max_segments <= kDecSegCap && bi.max_loras <= kDecLoraCap && p.num_tokens <= kDecPermCap;
+}
+
 bool qkv_split_pays(const LoraParams &p, const csgmv_batch_info &bi) {
     const int tm = token_tile(p, bi);
     // Vocabulary-wide outputs on 16- / 32-token tiles: the fused kernel gives
     // each tile's columns to one cluster, which leaves SMs idle and makes every
     // CTA stream tens of thousands of columns; with h in the workspace, the
     // expand-only launch spreads column blocks of every tile over all SMs.
-    if (tm <= 32) return p.off[p.c] - p.off[0] >= kWideCols;
+    // Other decode shapes: the split-K shrink and the expand of the decode
+    // kernels, which need no cluster barrier.
+    if (tm <= 32) return p.off[p.c] - p.off[0] >= kWideCols || decode_fits(p, bi);
     // 128-token tiles: the streaming tcgen05 shrink and expand
     return tm == 128 && p.R >= 16;
 }
 
+int qkv_max_parts(const LoraParams &p, const csgmv_batch_info &bi) {
+    return decode_fits(p, bi) ? kDecMaxParts : kMaxKParts;
+}
+
+int qkv_path(const LoraParams &p, const csgmv_batch_info &bi, size_t workspace_bytes) {
+    const size_t hbytes = (size_t)p.num_tokens * p.c * p.R * 4;
+    if (p.num_tokens <= 0 || workspace_bytes < kWsHeader + hbytes || !qkv_split_pays(p, bi)) return CSGMV_PATH_FUSED;
+    if (decode_fits(p, bi)) return CSGMV_PATH_DECODE;
+    if (token_tile(p, bi) == 128 && p.R >= 16) return CSGMV_PATH_STREAM;
+    return CSGMV_PATH_SMALL_SPLIT;
+}
+
+// The decode kernels (lora_decode.cuh) through the workspace: the split-K
+// shrink over one CTA per SM, then the expand as its programmatic dependent.
+cudaError_t launch_qkv_decode(LoraParams &ps, LoraParams &pe, const csgmv_batch_info &bi, cudaStream_t stream,
+                              void *workspace, size_t workspace_bytes) {
+    cudaError_t e = encoder();
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int L = bi.max_loras;
+    const int cR = ps.c * ps.R;
+    const size_t plane = (size_t)ps.num_tokens * ps.ldh;
+    const size_t room = workspace_bytes > kWsHeader ? workspace_bytes - kWsHeader : 0;
+    const int max_parts = (int)std::max<size_t>(1, std::min<size_t>(kDecMaxParts, plane ? room / (plane * 4) : 1));
+    float *planes = reinterpret_cast<float *>(static_cast<char *>(workspace) + kWsHeader);
+    const int nkc = (int)((ps.K + 63) / 64);
+
+    // ---- shrink: the table, then A boxes and x rows of up to kc_max chunks
+    DecodeParams ks;
+    memset(&ks, 0, sizeof ks);
+    ks.p = ps;
+    ks.p.h = planes;
+    ks.p.h_plane = (int64_t)plane;
+    ks.p.h_parts = max_parts;
+    ks.max_segments = bi.max_segments;
+    ks.tile_cap = (int)(csgmv_tile_table_ints(bi.max_loras, bi.max_tokens) / 4 - 1);
+    ks.nkc = nkc;
+    ks.shrink_grid = sms;
+    ks.a_rows = (int)align_up((size_t)cR, 16);
+    // the two kernels share an SM: shrink <= 100 KB, expand <= 120 KB
+    const size_t budget_s = 100 * 1024, budget_e = 120 * 1024;
+    size_t off = 0;
+    auto take = [&](size_t bytes, size_t align) {
+        off = align_up(off, align);
+        const size_t o = off;
+        off += bytes;
+        return (int)o;
+    };
+    ks.o_bar = take(16, 16);
+    ks.o_tab = take((size_t)kDecTabInts * 4, 16);
+    const size_t fixed_s = align_up(off, 1024) + 1024 + (size_t)kDecTM * 16 + 16;
+    const size_t per_chunk = (size_t)ks.a_rows * 128 + (size_t)kDecTM * 128;
+    ks.kc_max = (int)std::max<size_t>(1, std::min<size_t>(nkc, budget_s > fixed_s ? (budget_s - fixed_s) / per_chunk : 1));
+    ks.xpitch = ks.kc_max * 128 + 16;
+    ks.o_a = take((size_t)ks.kc_max * ks.a_rows * 128, 1024);
+    ks.o_x = take((size_t)kDecTM * ks.xpitch, 16);
+    const size_t smem_s = off + 1024;  // slack for aligning the window to 1024 bytes
+    if (!encode_2d(&ks.tmA, ps.A, (uint64_t)ps.K, (uint64_t)L * cR, (uint64_t)ps.K * 2, 64, ks.a_rows,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    ks.tmB = ks.tmA;
+    for (int j = 0; j < kMaxSlices; ++j) ks.tmBs[j] = ks.tmA;
+
+    // ---- expand: the table, base rows and B rows of up to cols_max columns, h
+    DecodeParams ke = ks;
+    ke.p = pe;
+    ke.p.h = planes;
+    ke.p.h_plane = (int64_t)plane;
+    ke.p.h_parts = max_parts;
+    const int rmax = pe.R <= 16 ? 16 : (pe.R <= 32 ? 32 : 64);
+    off = 0;
+    ke.o_bar = take(16, 16);
+    ke.o_tab = take((size_t)kDecTabInts * 4, 16);
+    // h as A fragments: slices x 16-row tiles x k16 steps x (hi, lo) x 512 bytes
+    const size_t hs_bytes = (size_t)kMaxSlices * (kDecTM / 16) * (rmax / 16) * 2 * 512;
+    const size_t fixed_e = align_up(off, 1024) + 1024 + hs_bytes + (size_t)kDecTM * 16 + 32;
+    const size_t per_blk = (size_t)kDecTM * 128 + (size_t)64 * pe.R * 2;
+    const int blks = (int)std::max<size_t>(1, std::min<size_t>(8, budget_e > fixed_e ? (budget_e - fixed_e) / per_blk : 1));
+    ke.cols_max = 64 * blks;
+    ke.ypitch = ke.cols_max * 2 + 16;
+    ke.o_y = take((size_t)kDecTM * ke.ypitch, 16);
+    ke.o_b = take((size_t)ke.cols_max * pe.R * 2, 1024);
+    ke.o_h = take(hs_bytes, 16);
+    const size_t smem_e = off + 1024;
+    if (!encode_b_maps(&ke.tmB, ke.tmBs, pe, L, 64)) return cudaErrorInvalidValue;
+    ke.tmA = ke.tmB;
+
+    const void *fs = lora_kernel_decode(0, rmax), *fe = lora_kernel_decode(1, rmax);
+    if (!fs || !fe) return cudaErrorInvalidValue;
+    if ((e = ensure_attrs(fs, dev, 1)) != cudaSuccess) return e;
+    if ((e = ensure_attrs(fe, dev, 1)) != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    set_dependent_launch(&attr[0]);
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kDecThreads, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(sms, 1, 1);
+    cfg.dynamicSmemBytes = smem_s;
+    void *args_s[1] = {&ks};
+    if ((e = cudaLaunchKernelExC(&cfg, fs, args_s)) != cudaSuccess) return e;
+    cfg.dynamicSmemBytes = smem_e;
+    cfg.blockDim = dim3(kDecExpThreads, 1, 1);
+    void *args_e[1] = {&ke};
+    if ((e = cudaLaunchKernelExC(&cfg, fe, args_e)) != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_qkv_split(LoraParams &ps, LoraParams &pe, const csgmv_batch_info &bi, cudaStream_t stream,
-                             void *workspace, size_t workspace_bytes) {
+                             void *workspace, size_t workspace_bytes, int path) {
+    if (path == CSGMV_PATH_DECODE) return launch_qkv_decode(ps, pe, bi, stream, workspace, workspace_bytes);
     // the workspace: a header (the part count), then planes of s * c * R floats
     int *header = static_cast<int *>(workspace);
     float *planes = reinterpret_cast<float *>(static_cast<char *>(workspace) + kWsHeader);
@@ -594,7 +723,7 @@ cudaError_t launch_qkv_split(LoraParams &ps, LoraParams &pe, const csgmv_batch_i
     pe.h = planes;
     pe.h_plane = (int64_t)plane;
     cudaError_t e;
-    if (token_tile(ps, bi) == 128 && ps.R >= 16) {
+    if (path == CSGMV_PATH_STREAM) {
         ps.h_plane = (int64_t)plane;
         e = launch_lora_sshrink(ps, bi, stream, nullptr, max_parts, header);
         pe.h_parts = max_parts;

@@ -54,6 +54,13 @@ def test_chunk_size_matches_rule_table(lib):
         assert binding.csgmv_chunk_size(n, mx) == want, (n, mx)
 
 
+def test_tile_table_size(lib):
+    from segmented_gather_gemm_gb300 import binding
+    for L, T in ((1, 0), (8, 256), (32, 35509), (256, 2048), (3, 63), (3, 64)):
+        assert binding.csgmv_tile_table_ints(L, T) == binding.tile_table_ints(L, T) == 4 * (L + T // 64 + 2)
+    assert binding.csgmv_tile_table_ints(-1, 4) == 0
+
+
 def test_capacity_matches_table(lib):
     from segmented_gather_gemm_gb300 import binding
     g = json.load(open(os.path.join(GOLDEN, "graph_capacity.json")))

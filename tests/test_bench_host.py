@@ -1,7 +1,8 @@
 """Host-side logic of bench.py that the JSON line depends on: the kernel count
-per csgmv_qkv call (gpu_launches mirrors the library's two-kernel choice), the
-algorithmic bytes of the decode line, and the source hash that keys the
-recorded DRAM traffic."""
+per csgmv_qkv call (gpu_launches: the library's own path choice, and the
+bench's rule for unbuilt batches checked against it), the algorithmic bytes
+of the decode line, and the source hash that keys the recorded DRAM
+traffic."""
 import os
 import shutil
 
@@ -23,12 +24,12 @@ SHAPES = {
 
 
 @pytest.mark.parametrize("name, kernels", [
-    ("decode_qkv", 1),         # 32-token tiles, 6144 columns: one fused kernel
+    ("decode_qkv", 2),         # 32-token tiles, 6144 columns: the decode shrink and expand
     ("prefill_gate_up", 2),    # 128-token tiles: shrink into the workspace, then expand
     ("skewed_down_proj", 2),   # 128-token tiles, K = 14336: the same two kernels
     ("lm_head_decode", 2),     # 16-token tiles, 128256 columns: the vocabulary-wide split
     ("lm_head_pruned", 2),
-    ("tiny", 1),
+    ("tiny", 2),               # 21 tokens per slot: the decode shrink and expand
 ])
 def test_kernels_per_call(name, kernels):
     assert bench.qkv_kernels(SHAPES[name](), None) == kernels
@@ -38,11 +39,53 @@ def test_embedding_is_one_kernel():
     assert bench.qkv_kernels(wl.embedding_gather(n_req=2, req_len=4, V=64), None) == 1
 
 
-def test_wide_split_threshold():
-    """The two-kernel path for small tiles starts at WIDE_COLS output columns."""
-    for cols, kernels in ((bench.WIDE_COLS - 8, 1), (bench.WIDE_COLS, 2)):
+@pytest.fixture(scope="module")
+def lib():
+    from segmented_gather_gemm_gb300 import build as sgb
+    try:
+        sgb.build()
+    except RuntimeError as e:  # no nvcc on this machine
+        pytest.skip(str(e))
+    from segmented_gather_gemm_gb300 import binding
+    return binding
+
+
+def cpu_batch(B, w, max_segments=None):
+    """A batch info with the bench's capacities (max_segments = tokens + 1
+    unless given) and the host mirror of workload w, in host memory: enough
+    for csgmv_qkv_path, which reads no device buffer."""
+    bi = B.BatchInfo(max(w.bs, 1), w.s, w.s + 1 if max_segments is None else max_segments, max_loras=w.L,
+                     max_rank=w.R, device="cpu")
+    bi.c.num_tokens, bi.c.bs, bi.c.num_loras, bi.c.chunk_size = w.s, w.bs, w.L, 16
+    return bi
+
+
+@pytest.mark.parametrize("name", sorted(SHAPES))
+def test_rule_matches_library_path(lib, name):
+    w = SHAPES[name]()
+    assert bench.qkv_kernels(w, None) == bench.qkv_kernels(w, cpu_batch(lib, w))
+
+
+def test_library_paths_of_the_workloads(lib):
+    want = {"decode_qkv": "decode", "prefill_gate_up": "stream", "skewed_down_proj": "stream",
+            "lm_head_decode": "small_split", "lm_head_pruned": "small_split", "tiny": "decode"}
+    for name, path in want.items():
+        w = SHAPES[name]()
+        bi = cpu_batch(lib, w)
+        ws = lib.csgmv_qkv_workspace_bytes(bi, w.c)
+        assert lib.csgmv_qkv_path(bi, w.K, w.N, w.offsets, w.c, ws) == path, name
+        assert lib.csgmv_qkv_path(bi, w.K, w.N, w.offsets, w.c, 0) == "fused", name
+
+
+def test_small_tile_split_rules(lib):
+    """Small tiles take two kernels either way within the decode kernels'
+    table capacities; beyond them, only from WIDE_COLS output columns."""
+    for cols, kernels, ms in ((bench.WIDE_COLS - 8, 2, None), (bench.WIDE_COLS, 2, None),
+                              (bench.WIDE_COLS - 8, 1, 4096), (bench.WIDE_COLS, 2, 4096)):
         w = wl.random_lora(3, bs=40, max_len=1, K=64, N_slices=[cols], R=16, L=6, min_len=1)
-        assert bench.qkv_kernels(w, None) == kernels
+        assert bench.qkv_kernels(w, cpu_batch(lib, w, ms)) == kernels
+        if ms is None:
+            assert bench.qkv_kernels(w, None) == kernels
 
 
 def test_decode_algorithmic_bytes():
@@ -76,8 +119,8 @@ def test_source_hash_ignores_comments(tmp_path, monkeypatch):
 
 
 def test_source_hash_is_per_workload(tmp_path, monkeypatch):
-    """A change to the small-tile kernel drops the decode and lm_head records
-    but keeps the prefill one, whose kernels do not include it."""
+    """A change to the small-tile kernel drops the lm_head record but keeps
+    the decode and prefill ones, whose kernels do not include it."""
     csrc = os.path.join(bench.ROOT, "segmented_gather_gemm_gb300", "csrc")
     root = tmp_path / "repo"
     shutil.copytree(csrc, root / "segmented_gather_gemm_gb300" / "csrc")
@@ -87,5 +130,5 @@ def test_source_hash_is_per_workload(tmp_path, monkeypatch):
     f.write_text(f.read_text().replace("#pragma once", "#pragma once\nconstexpr int kUnused = 1;", 1))
     after = {w: bench.kernel_source_hash(w) for w in bench.KERNEL_SOURCES}
     assert after["prefill_gate_up"] == before["prefill_gate_up"]
-    assert after["decode_qkv"] != before["decode_qkv"]
+    assert after["decode_qkv"] == before["decode_qkv"]
     assert after["lm_head_decode"] != before["lm_head_decode"]

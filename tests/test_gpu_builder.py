@@ -53,6 +53,30 @@ def compare(bi, lens, adapter, chunk, graph=False):
     bs = len(lens)
     assert np.array_equal(bi.req_seg_indptr[:bs + 1].cpu().numpy(), ref["req_seg_indptr"])
     assert np.array_equal(bi.req_weight_indices[:bs].cpu().numpy(), ref["req_weight_indices"])
+    want = expected_tiles(ref)
+    got = bi.tile_table.cpu().numpy()
+    assert int(got[0]) == len(want) and not got[1:4].any()
+    assert np.array_equal(got[4:4 + 4 * len(want)].reshape(-1, 4), np.array(want, np.int32).reshape(-1, 4))
+
+
+def expected_tiles(ref, tm=64):
+    """Decode tiles from the oracle's segments: each maximal stretch of
+    segments on one slot (a slot run of n tokens) cut into ceil(n / tm)
+    tiles of balanced size, records (slot, first position, tokens, 0)."""
+    n = ref["num_segments"]
+    w, ip = ref["weight_indices"][:n], ref["seg_indptr"][:n + 1]
+    tiles, k = [], 0
+    while k < n:
+        e = k
+        while e + 1 < n and w[e + 1] == w[k]:
+            e += 1
+        p0, cnt = int(ip[k]), int(ip[e + 1] - ip[k])
+        nt = -(-cnt // tm)
+        for i in range(nt):
+            lo, hi = i * cnt // nt, (i + 1) * cnt // nt
+            tiles.append((int(w[k]), p0 + lo, hi - lo, 0))
+        k = e + 1
+    return tiles
 
 
 def test_tiny_golden():

@@ -1,12 +1,13 @@
 """The named workloads at their full sizes, each through the csgmv_qkv path
 the benchmark times.  The benchmark passes an h workspace to every
-csgmv_qkv call, so the library takes its two-kernel path (shrink into the
-fp32 workspace, then an expand-only launch) wherever that is its choice:
-prefill gate_up (128-token tiles, K <= 4096) and both lm_head workloads
-(vocabulary-wide outputs on 16-token tiles).  Decode QKV and skewed
-down_proj run the one-kernel fused path either way.  Each test asserts which
-path its call takes, with the same rule the benchmark uses to count kernel
-launches.
+csgmv_qkv call, so the library takes a two-kernel path (a shrink into the
+fp32 workspace, then an expand) wherever that is its choice: decode QKV (the
+cluster-free decode kernels), prefill gate_up and skewed down_proj (the
+streaming tcgen05 shrink and expand on 128-token tiles) and both lm_head
+workloads (vocabulary-wide outputs on 16-token tiles: the small-tile shrink
+and expand-only launches).  The decode QKV and lm_head decode tests also run
+the one-kernel fused path (no workspace).  Each test asserts how many kernels its call
+launches, with the same rule the benchmark uses to count them.
 
 Decode and lm_head are compared element by element; the prefill workloads on
 sampled token rows (every column of each sampled row), which the oracle
@@ -36,13 +37,17 @@ def sample_rows(w, n=192, seed=0):
     return np.array(sorted(rows))
 
 
-def test_decode_qkv_full():
+@pytest.mark.parametrize("workspace", [True, False], ids=["workspace", "on-chip"])
+def test_decode_qkv_full(workspace):
+    """bs 256 x 1 token on 8 slots: with a workspace (the benchmark's call)
+    the decode shrink and expand, without one the fused cluster kernel."""
     w = wl.decode_qkv()
     for base in (True, False):
-        y, bi = run_fused(w, base=base, workspace=True)
-        assert bench.qkv_kernels(w, bi) == 1
+        y, bi = run_fused(w, base=base, workspace=workspace)
+        if workspace:
+            assert bench.qkv_kernels(w, bi) == 2
         assert bi.device_status() == 0
-        assert_close(f64(y), oracle_fused(w, base=base), f"decode qkv base={base}")
+        assert_close(f64(y), oracle_fused(w, base=base), f"decode qkv base={base} workspace={workspace}")
 
 
 @pytest.mark.parametrize("workspace", [True, False], ids=["workspace", "on-chip"])

@@ -61,6 +61,7 @@ def test_lm_head_hand_derived():
     assert bi.permutation[:11].cpu().tolist() == g["permutation"]
     assert bi.weight_indices[:6].cpu().tolist() == g["graph_weight_indices"]
     assert bi.seg_indptr[:7].cpu().tolist() == g["graph_seg_indptr"]
+    assert int(bi.tile_table[0].item()) == -1  # no decode tiles from this builder
 
 
 @pytest.mark.parametrize("seed", range(8))
