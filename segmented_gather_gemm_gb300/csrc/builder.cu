@@ -396,6 +396,13 @@ build_lm_head_kernel(BuildParams p, csgmv_batch_info bi) {
     const int err = flags[0];
     // no tile table: the decode kernels derive tiles from the segments
     if (tid == 0 && bi.tile_table) bi.tile_table[0] = -1;
+    // per-request fields: first pruned token and slot of every request
+    if (!err) {
+        if (bi.req_seg_indptr)
+            for (int i = tid; i <= p.bs; i += kBuildThreads) bi.req_seg_indptr[i] = req_start[i];
+        if (bi.req_weight_indices)
+            for (int i = tid; i < p.bs; i += kBuildThreads) bi.req_weight_indices[i] = p.req_adapter[i];
+    }
     if (err) {
         if (tid == 0) {
             *bi.num_segments_dev = 0;

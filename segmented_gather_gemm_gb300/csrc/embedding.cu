@@ -105,6 +105,90 @@ embedding_lora_a_kernel(EmbeddingParams p, const int32_t *__restrict__ seg_indpt
     }
 }
 
+// Token-major gather for batch infos with per-request fields (every batch
+// info from either builder, when the caller allocated those fields): the
+// token's slot is its request's, so a block of kTokPerBlock consecutive
+// tokens loads, in one round, their ids together with the request starts,
+// request slots and slot ranks; lanes 0..7 of each warp find their token's
+// request by binary search in shared memory, and then every lane gathers its
+// rank column of the warp's eight tokens.  Two dependent rounds of memory
+// (ids, then the table) instead of five (segments, token, id, table).
+constexpr int kTokThreads = 256;
+constexpr int kTokWarps = kTokThreads / 32;
+constexpr int kTokPerWarp = 8;
+constexpr int kTokPerBlock = kTokWarps * kTokPerWarp;
+
+__global__ void __launch_bounds__(kTokThreads)
+embedding_token_kernel(EmbeddingParams p, const int32_t *__restrict__ req_start_g, const int32_t *__restrict__ req_slot_g,
+                       int bs, const int32_t *__restrict__ ranks, int nl, const int32_t *__restrict__ nseg_dev,
+                       int32_t *status) {
+    extern __shared__ int sm_tok[];
+    int *st = sm_tok;        // [bs + 1] first token of request i
+    int *sl = st + bs + 1;   // [bs] slot of request i
+    int *rk = sl + bs;       // [nl] slot ranks
+    griddep_wait();  // the batch info may come from the kernel launched just before
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i <= bs; i += kTokThreads) {
+        st[i] = req_start_g[i];
+        if (i < bs) sl[i] = req_slot_g[i];
+    }
+    for (int a = tid; a < nl; a += kTokThreads) rk[a] = ranks[a];
+    const int nseg = *nseg_dev;
+    const int t0 = blockIdx.x * kTokPerBlock + warp * kTokPerWarp;
+    // lane u < 8 owns token t0 + u: its id, then its slot and rank
+    const int tu = t0 + lane;
+    int64_t my_id = -1;
+    if (lane < kTokPerWarp && tu < p.num_tokens) my_id = p.ids[tu];
+    __syncthreads();
+    if (nseg <= 0) return;  // the build failed (or the batch is empty): nothing is written, as in the segment kernel
+    int my_w = -1, my_r = 0;
+    if (lane < kTokPerWarp && tu < p.num_tokens) {
+        int lo = 0, hi = bs;  // last request with start <= tu
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (st[mid] <= tu) lo = mid; else hi = mid;
+        }
+        const int w = sl[lo];
+        if (w < 0 || w >= p.max_loras || w >= nl) {
+            atomicOr(status, CSGMV_STATUS_BAD_ADAPTER);
+        } else {
+            const int r = rk[w];
+            if (r < 0 || r > p.R) atomicOr(status, CSGMV_STATUS_BAD_RANK);
+            else { my_w = w; my_r = r; }
+        }
+        if (my_id < 0 || my_id >= p.V + p.E) {
+            atomicOr(status, CSGMV_STATUS_BAD_TOKEN_ID);
+            my_id = -1;
+        }
+        if (my_w < 0) my_id = -1;
+    }
+    int64_t id[kTokPerWarp];
+    int w[kTokPerWarp], r[kTokPerWarp];
+#pragma unroll
+    for (int u = 0; u < kTokPerWarp; ++u) {
+        id[u] = __shfl_sync(0xffffffffu, my_id, u);
+        w[u] = __shfl_sync(0xffffffffu, my_w, u);
+        r[u] = __shfl_sync(0xffffffffu, my_r, u);
+    }
+    for (int k0 = 0; k0 < p.R; k0 += 32) {
+        const int k = k0 + lane;
+        uint16_t v[kTokPerWarp];
+#pragma unroll
+        for (int u = 0; u < kTokPerWarp; ++u) {
+            v[u] = 0;
+            if (id[u] >= 0 && k < r[u])
+                v[u] = id[u] < p.V ? __ldg(p.A + ((int64_t)w[u] * p.R + k) * p.V + id[u])
+                                   : __ldg(p.extra + ((int64_t)w[u] * p.E + (id[u] - p.V)) * p.R + k);
+        }
+#pragma unroll
+        for (int u = 0; u < kTokPerWarp; ++u)
+            if (t0 + u < p.num_tokens && k < p.R) p.out[(int64_t)(t0 + u) * p.R + k] = v[u];
+    }
+}
+
+constexpr int kTokReqCap = 4096;  // requests whose table fits the token-major kernel's shared memory
+constexpr int kTokLoraCap = 4096;
+
 // Rows of extra tokens of an (s, D) output become extra[w][id - V][:].  Each
 // lane checks one token of the warp's slice; the warp then copies the rows of
 // the lanes that hold an extra token, one row at a time, 16 bytes per lane.
@@ -184,6 +268,20 @@ cudaLaunchConfig_t item_config(const csgmv_batch_info &bi, int spp, cudaStream_t
 }  // namespace
 
 cudaError_t launch_embedding(const EmbeddingParams &p, const csgmv_batch_info &bi, cudaStream_t stream) {
+    if (bi.req_seg_indptr && bi.req_weight_indices && bi.bs >= 1 && bi.bs <= kTokReqCap &&
+        bi.max_loras <= kTokLoraCap && p.num_tokens > 0) {
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = item_config(bi, 1, stream, attr);
+        cfg.gridDim = dim3((p.num_tokens + kTokPerBlock - 1) / kTokPerBlock, 1, 1);
+        cfg.blockDim = dim3(kTokThreads, 1, 1);
+        cfg.dynamicSmemBytes = sizeof(int) * (2 * (size_t)bi.bs + 1 + (size_t)bi.max_loras);
+        cudaError_t e = cudaLaunchKernelEx(&cfg, embedding_token_kernel, p, (const int32_t *)bi.req_seg_indptr,
+                                           (const int32_t *)bi.req_weight_indices, (int)bi.bs,
+                                           (const int32_t *)bi.lora_ranks, (int)bi.max_loras,
+                                           (const int32_t *)bi.num_segments_dev, (int32_t *)bi.status);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     // One block row per segment slot, and enough token slices to cover a
     // segment of chunk_size tokens.
     const int chunk = bi.chunk_size > 0 ? bi.chunk_size : kMinChunkSize;

@@ -6,7 +6,7 @@ import torch
 import oracle
 from segmented_gather_gemm_gb300 import binding as B
 from segmented_gather_gemm_gb300 import workloads as wl
-from tests.gpu_helpers import build_batch, dev_bf16, dev_i32, host_bits
+from tests.gpu_helpers import build_batch, dev_bf16, dev_f32, dev_i32, host_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -122,3 +122,29 @@ def test_extra_token_embedding_rows(D):
     ta = oracle.token_adapter(e.req_lens, e.req_adapter)
     ref, bad = oracle.extra_token_embedding(ids, output, extra, e.V, ta)
     assert bad == 0 and np.array_equal(host_bits(y), ref)
+
+
+def test_token_major_and_segment_kernels_agree():
+    """With per-request fields in the batch info the gather is token-major;
+    without them it walks the segments.  Both give the oracle's bits, also
+    with extra tokens and ragged ranks."""
+    e = wl.embedding_gather(seed=21, n_req=9, req_len=70, V=3000, R=40, L=5)
+    e.req_lens = np.array([70, 0, 200, 3, 70, 1, 17, 64, 65], np.int32)
+    e.ids = np.random.default_rng(4).integers(0, 3000, size=e.s).astype(np.int32)
+    e.ranks[:] = [40, 0, 17, 39, 8]
+    ids, extra = _with_extra(e, 11, 0.2, 5)
+    lens, ad = dev_i32(e.req_lens), dev_i32(e.req_adapter)
+    ranks, scal = dev_i32(e.ranks), dev_f32(np.ones(e.L, np.float32))
+    outs = []
+    for with_req in (True, False):
+        bi = B.BatchInfo.for_batch(len(e.req_lens), e.s, e.L, e.R, with_request_fields=with_req)
+        B.csgmv_build_batch_info(bi, lens, ad, e.s, ranks, scal)
+        out = torch.full((e.s, e.R), 5.0, dtype=torch.bfloat16, device="cuda")
+        B.embedding_lora_a_extra(dev_i32(ids), dev_bf16(e.A_emb), e.V, dev_bf16(extra), out, bi)
+        torch.cuda.synchronize()
+        assert bi.device_status() == 0
+        outs.append(host_bits(out))
+    ta = oracle.token_adapter(e.req_lens, e.req_adapter)
+    ref, bad = oracle.embedding_extra(ids, e.A_emb, extra, ta, e.ranks)
+    assert bad == 0
+    assert np.array_equal(outs[0], ref) and np.array_equal(outs[1], ref)

@@ -62,6 +62,10 @@ def test_lm_head_hand_derived():
     assert bi.weight_indices[:6].cpu().tolist() == g["graph_weight_indices"]
     assert bi.seg_indptr[:7].cpu().tolist() == g["graph_seg_indptr"]
     assert int(bi.tile_table[0].item()) == -1  # no decode tiles from this builder
+    # per-request fields: first pruned token and slot of every request
+    starts = np.concatenate([[0], np.cumsum(g["pruned_lens"])])
+    assert bi.req_seg_indptr[:len(starts)].cpu().tolist() == starts.tolist()
+    assert bi.req_weight_indices[:len(g["req_adapter"])].cpu().tolist() == list(g["req_adapter"])
 
 
 @pytest.mark.parametrize("seed", range(8))
