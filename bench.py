@@ -55,6 +55,7 @@ PER_CONFIG = [
     ("lm_head_decode", "lm_head_decode", 0),
     ("lm_head_pruned", "lm_head_pruned", 0),
     ("embedding", "embedding", 0),
+    ("embedding_transposed", "embedding_transposed", 0),
 ]
 TARGET_FRAC = {"prefill_gate_up": 0.70, "skewed_down_proj": 0.70, "decode_qkv": 0.60, "lm_head_decode": 0.60}
 
@@ -76,6 +77,11 @@ def make_workload(name: str, seed: int, chunk: int, scale: float = 1.0, bs: int 
         return wl.tiny_single_slice(seed=seed)
     if name == "embedding":
         return wl.embedding_gather(seed=seed)
+    if name == "embedding_transposed":  # the same gather from the load-time (L, V, R) table
+        w = wl.embedding_gather(seed=seed)
+        w.transposed = True
+        w.name = w.name.replace("embedding_lora_a", "embedding_lora_a_transposed")
+        return w
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -277,7 +283,9 @@ class DeviceSet:
         if isinstance(w, wl.EmbeddingWorkload):
             self.scal = torch.ones(w.L, dtype=torch.float32, device="cuda")
             self.ids = share.ids if share else torch.from_numpy(w.ids).cuda()
-            self.A = share.A if share else bf(w.A_emb)
+            # the transposed table is made once, as a caller does when it loads an adapter
+            self.A = share.A if share else (B.csgmv_transpose_embedding(bf(w.A_emb)) if w.transposed
+                                            else bf(w.A_emb))
             self.out = torch.zeros((w.s, w.R), dtype=torch.bfloat16, device="cuda")
             self.bi = B.BatchInfo.for_batch(len(w.req_lens), w.s, w.L, w.R)
         else:
@@ -311,7 +319,10 @@ class DeviceSet:
         from segmented_gather_gemm_gb300 import binding as B
         w = self.w
         if isinstance(w, wl.EmbeddingWorkload):
-            B.embedding_lora_a(self.ids, self.A, w.V, self.out, self.bi)
+            if w.transposed:
+                B.embedding_lora_a_transposed(self.ids, self.A, w.V, None, self.out, self.bi)
+            else:
+                B.embedding_lora_a(self.ids, self.A, w.V, self.out, self.bi)
         else:
             B.csgmv_qkv(self.x, self.A, self.B, w.offsets, w.c, self.widest, self.y, self.bi, workspace=self.ws)
 
@@ -746,7 +757,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_gate_up",
                     choices=["decode_qkv", "prefill_gate_up", "skewed_down_proj", "lm_head_decode", "lm_head_pruned",
-                             "tiny", "embedding"])
+                             "tiny", "embedding", "embedding_transposed"])
     ap.add_argument("--chunk", type=int, default=128, help="chunk size of skewed_down_proj")
     ap.add_argument("--scale", type=float, default=1.0, help="token scale of the prefill workloads")
     ap.add_argument("--bs", type=int, default=0, help="requests of the decode workloads (0 = default)")

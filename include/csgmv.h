@@ -362,6 +362,29 @@ CSGMV_API int embedding_lora_a_extra(const int32_t *input_ids, const void *A_emb
                                      const csgmv_batch_info *bi, csgmv_stream_t stream);
 
 /*
+ * embedding_lora_a_extra with A_emb stored transposed: A_emb_t bf16
+ * (max_loras, vocab_size, rank), A_emb_t[w][id][k] = A_emb[w][k][id].  The
+ * (max_loras, rank, vocab_size) layout of the pages puts each of a token's
+ * rank values in its own 32-byte memory sector; here they are one
+ * contiguous row, so the gather reads rank * 2 bytes per token instead of
+ * rank sectors.  A caller transposes each adapter once when it loads it
+ * (csgmv_transpose_embedding).  Results are identical to
+ * embedding_lora_a_extra on the untransposed table.  An addition of this
+ * library (the load-time layout is not on the pages).
+ */
+CSGMV_API int embedding_lora_a_transposed(const int32_t *input_ids, const void *A_emb_t, int64_t vocab_size,
+                                          int rank, const void *extra_embeddings, int64_t num_extra_tokens,
+                                          void *out, const csgmv_batch_info *bi, csgmv_stream_t stream);
+
+/*
+ * A_emb_t[w][v][k] = A_emb[w][k][v] for w < num_loras (both bf16, device):
+ * the load-time layout of embedding_lora_a_transposed.  Asynchronous on
+ * stream; the two buffers must not overlap.  1 <= rank <= 1024.
+ */
+CSGMV_API int csgmv_transpose_embedding(const void *A_emb, int64_t num_loras, int rank, int64_t vocab_size,
+                                        void *A_emb_t, csgmv_stream_t stream);
+
+/*
  * Extra-token embedding (base_backend.py run_extra_token_embedding): in the
  * (s, embed_dim) output of the base embedding, the row of every token t on
  * slot w with vocab_size <= id < vocab_size + num_extra_tokens becomes

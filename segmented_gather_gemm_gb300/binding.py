@@ -24,7 +24,8 @@ STATUS_BITS = {
 EXPORTED = ["csgmv_last_error", "csgmv_version", "csgmv_chunk_size", "csgmv_batch_info_capacity",
             "csgmv_build_batch_info", "csgmv_build_lm_head_batch_info", "csgmv_shrink", "csgmv_expand", "csgmv_qkv", "csgmv_qkv_workspace_bytes",
             "csgmv_qkv_static_scratch", "embedding_lora_a", "embedding_lora_a_extra", "extra_token_embedding",
-            "csgmv_expand_sliced", "csgmv_qkv_sliced", "csgmv_qkv_path", "csgmv_tile_table_ints"]
+            "csgmv_expand_sliced", "csgmv_qkv_sliced", "csgmv_qkv_path", "csgmv_tile_table_ints",
+            "embedding_lora_a_transposed", "csgmv_transpose_embedding"]
 
 # csgmv_qkv_path results (CSGMV_PATH_*)
 PATHS = {0: "fused", 1: "decode", 2: "small_split", 3: "stream"}
@@ -81,6 +82,8 @@ def lib():
         "extra_token_embedding": (i32, [vp, vp, i64, vp, i64, i64, bip, vp]),
         "csgmv_qkv_path": (i32, [bip, i64, i64, i32p, i32, ctypes.c_size_t]),
         "csgmv_tile_table_ints": (i64, [i32, i32]),
+        "embedding_lora_a_transposed": (i32, [vp, vp, i64, i32, vp, i64, vp, bip, vp]),
+        "csgmv_transpose_embedding": (i32, [vp, i64, i32, i64, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -288,6 +291,26 @@ def embedding_lora_a_extra(input_ids: torch.Tensor, A_emb: torch.Tensor, vocab_s
     _check(lib().embedding_lora_a_extra(_ptr(input_ids), _ptr(A_emb), int(vocab_size), int(out.shape[1]),
                                         _ptr(extra_embeddings), E, _ptr(out), ctypes.byref(bi.c), _stream(stream)))
     return out
+
+
+def embedding_lora_a_transposed(input_ids: torch.Tensor, A_emb_t: torch.Tensor, vocab_size: int,
+                                extra_embeddings: torch.Tensor | None, out: torch.Tensor, bi: BatchInfo,
+                                stream=None) -> torch.Tensor:
+    """embedding_lora_a_extra with the table stored as A_emb_t (L, V, R)."""
+    E = 0 if extra_embeddings is None else int(extra_embeddings.shape[1])
+    _check(lib().embedding_lora_a_transposed(_ptr(input_ids), _ptr(A_emb_t), int(vocab_size), int(out.shape[1]),
+                                             _ptr(extra_embeddings), E, _ptr(out), ctypes.byref(bi.c),
+                                             _stream(stream)))
+    return out
+
+
+def csgmv_transpose_embedding(A_emb: torch.Tensor, A_emb_t: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """A_emb_t (L, V, R) from A_emb (L, R, V), on the device (load time)."""
+    L, R, V = (int(v) for v in A_emb.shape)
+    if A_emb_t is None:
+        A_emb_t = torch.empty((L, V, R), dtype=A_emb.dtype, device=A_emb.device)
+    _check(lib().csgmv_transpose_embedding(_ptr(A_emb), L, R, V, _ptr(A_emb_t), _stream(stream)))
+    return A_emb_t
 
 
 def extra_token_embedding(input_ids: torch.Tensor, output: torch.Tensor, extra_embeddings: torch.Tensor,

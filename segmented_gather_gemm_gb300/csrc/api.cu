@@ -263,6 +263,10 @@ int qkv_impl(const void *x, int64_t K, const void *A, const void *B, const void 
     return CSGMV_OK;
 }
 
+int embedding_impl(const int32_t *input_ids, const void *A_emb, int transposed, int64_t vocab_size, int rank,
+                   const void *extra_embeddings, int64_t num_extra_tokens, void *out, const csgmv_batch_info *bi,
+                   csgmv_stream_t stream);
+
 }  // namespace
 
 extern "C" {
@@ -477,6 +481,38 @@ int embedding_lora_a(const int32_t *input_ids, const void *A_emb, int64_t vocab_
 int embedding_lora_a_extra(const int32_t *input_ids, const void *A_emb, int64_t vocab_size, int rank,
                            const void *extra_embeddings, int64_t num_extra_tokens, void *out,
                            const csgmv_batch_info *bi, csgmv_stream_t stream) {
+    return embedding_impl(input_ids, A_emb, 0, vocab_size, rank, extra_embeddings, num_extra_tokens, out, bi, stream);
+}
+
+int embedding_lora_a_transposed(const int32_t *input_ids, const void *A_emb_t, int64_t vocab_size, int rank,
+                                const void *extra_embeddings, int64_t num_extra_tokens, void *out,
+                                const csgmv_batch_info *bi, csgmv_stream_t stream) {
+    return embedding_impl(input_ids, A_emb_t, 1, vocab_size, rank, extra_embeddings, num_extra_tokens, out, bi,
+                          stream);
+}
+
+int csgmv_transpose_embedding(const void *A_emb, int64_t num_loras, int rank, int64_t vocab_size, void *A_emb_t,
+                              csgmv_stream_t stream) {
+    if (num_loras < 0 || rank < 1 || rank > 1024 || vocab_size <= 0)
+        return fail(CSGMV_ERR_INVALID_ARG, "num_loras >= 0, 1 <= rank <= 1024 and vocab_size > 0 required");
+    if (num_loras == 0) return CSGMV_OK;
+    if (!A_emb || !A_emb_t) return fail(CSGMV_ERR_INVALID_ARG, "NULL tensor");
+    const size_t bytes = (size_t)num_loras * rank * vocab_size * 2;
+    if (overlaps(A_emb, bytes, A_emb_t, bytes)) return fail(CSGMV_ERR_INVALID_ARG, "A_emb_t overlaps A_emb");
+    cudaError_t e = csgmv::launch_transpose_embedding(static_cast<const uint16_t *>(A_emb), num_loras, rank,
+                                                      vocab_size, static_cast<uint16_t *>(A_emb_t),
+                                                      reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "csgmv_transpose_embedding launch");
+    return CSGMV_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+int embedding_impl(const int32_t *input_ids, const void *A_emb, int transposed, int64_t vocab_size, int rank,
+                   const void *extra_embeddings, int64_t num_extra_tokens, void *out, const csgmv_batch_info *bi,
+                   csgmv_stream_t stream) {
     int rc = check_bi(bi, true);
     if (rc) return rc;
     if (rank < 1 || rank > 1024) return fail(CSGMV_ERR_UNSUPPORTED, "rank %d not in [1, 1024]", rank);
@@ -494,6 +530,7 @@ int embedding_lora_a_extra(const int32_t *input_ids, const void *A_emb, int64_t 
     csgmv::EmbeddingParams p;
     p.ids = input_ids;
     p.A = static_cast<const uint16_t *>(A_emb);
+    p.transposed = transposed;
     p.extra = num_extra_tokens > 0 ? static_cast<const uint16_t *>(extra_embeddings) : nullptr;
     p.out = static_cast<uint16_t *>(out);
     p.V = vocab_size;
@@ -505,6 +542,10 @@ int embedding_lora_a_extra(const int32_t *input_ids, const void *A_emb, int64_t 
     if (e != cudaSuccess) return cuda_fail(e, "embedding_lora_a launch");
     return CSGMV_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 int extra_token_embedding(const int32_t *input_ids, void *output, int64_t embed_dim, const void *extra_embeddings,
                           int64_t num_extra_tokens, int64_t vocab_size, const csgmv_batch_info *bi,

@@ -118,7 +118,8 @@ cudaError_t launch_build_lm_head(const BuildParams &p, const csgmv_batch_info &b
 // embedding.cu
 struct EmbeddingParams {
     const int32_t *ids;
-    const uint16_t *A;      // (max_loras, R, V)
+    const uint16_t *A;      // (max_loras, R, V), or (max_loras, V, R) when transposed
+    int transposed;         // 1: A is (max_loras, V, R), one contiguous row of R per id
     const uint16_t *extra;  // (max_loras, E, R) rows of extra tokens, or NULL (E = 0)
     uint16_t *out;          // (s, R)
     int64_t V, E;
@@ -126,6 +127,9 @@ struct EmbeddingParams {
     int num_tokens, max_loras;
 };
 cudaError_t launch_embedding(const EmbeddingParams &p, const csgmv_batch_info &bi, cudaStream_t stream);
+// out (L, V, R) = A (L, R, V) transposed per slot.
+cudaError_t launch_transpose_embedding(const uint16_t *A, int64_t L, int R, int64_t V, uint16_t *out,
+                                       cudaStream_t stream);
 struct ExtraTokenParams {
     const int32_t *ids;
     const uint16_t *extra;  // (max_loras, E, D)

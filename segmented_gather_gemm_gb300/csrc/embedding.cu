@@ -16,6 +16,11 @@
 namespace csgmv {
 namespace {
 
+// A_emb[w][k][id]: (L, R, V), or (L, V, R) for the transposed layout.
+__device__ __forceinline__ uint16_t emb_at(const EmbeddingParams &p, int w, int k, int64_t id) {
+    return p.transposed ? __ldg(p.A + ((int64_t)w * p.V + id) * p.R + k) : __ldg(p.A + ((int64_t)w * p.R + k) * p.V + id);
+}
+
 constexpr int kEmbThreads = 128;
 constexpr int kEmbWarps = kEmbThreads / 32;
 
@@ -62,7 +67,6 @@ embedding_lora_a_kernel(EmbeddingParams p, const int32_t *__restrict__ seg_indpt
     for (int seg = blockIdx.x; seg < nseg; seg += gridDim.x) {
         const SegInfo g = seg_info(seg, p.num_tokens, p.max_loras, p.R, seg_indptr, weight_indices, ranks, status,
                                    threadIdx.x == 0 && blockIdx.y == 0);
-        const uint16_t *Aw = p.A + (int64_t)(g.ok ? g.w : 0) * p.R * p.V;
         const uint16_t *Ew = p.extra ? p.extra + (int64_t)(g.ok ? g.w : 0) * p.E * p.R : nullptr;
         const int step = gridDim.y * kTokPerIter;
         for (int pb = g.p0 + blockIdx.y * kTokPerIter * kUnroll; pb < g.p1; pb += step * kUnroll) {
@@ -95,7 +99,7 @@ embedding_lora_a_kernel(EmbeddingParams p, const int32_t *__restrict__ seg_indpt
                 for (int u = 0; u < kUnroll; ++u) {
                     v[u] = 0;
                     if (id[u] >= 0 && k < g.r)
-                        v[u] = id[u] < p.V ? __ldg(Aw + (int64_t)k * p.V + id[u]) : __ldg(Ew + (id[u] - p.V) * p.R + k);
+                        v[u] = id[u] < p.V ? emb_at(p, g.ok ? g.w : 0, k, id[u]) : __ldg(Ew + (id[u] - p.V) * p.R + k);
                 }
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u)
@@ -177,7 +181,7 @@ embedding_token_kernel(EmbeddingParams p, const int32_t *__restrict__ req_start_
         for (int u = 0; u < kTokPerWarp; ++u) {
             v[u] = 0;
             if (id[u] >= 0 && k < r[u])
-                v[u] = id[u] < p.V ? __ldg(p.A + ((int64_t)w[u] * p.R + k) * p.V + id[u])
+                v[u] = id[u] < p.V ? emb_at(p, w[u], k, id[u])
                                    : __ldg(p.extra + ((int64_t)w[u] * p.E + (id[u] - p.V)) * p.R + k);
         }
 #pragma unroll
@@ -240,6 +244,29 @@ extra_token_kernel(ExtraTokenParams p, const int32_t *__restrict__ seg_indptr,
     }
 }
 
+// out[w][v][k] = A[w][k][v]: 32 x 32 tiles through shared memory (the +1
+// column keeps the transposed reads free of bank conflicts); grid (V / 32,
+// R / 32, L) rounded up.
+__global__ void __launch_bounds__(256) transpose_embedding_kernel(const uint16_t *__restrict__ A, int R, int64_t V,
+                                                                  uint16_t *__restrict__ out) {
+    __shared__ uint16_t tile[32][33];
+    const int64_t v0 = (int64_t)blockIdx.x * 32;
+    const int k0 = blockIdx.y * 32;
+    const int64_t w = blockIdx.z;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 8 rows of 32
+    for (int i = ty; i < 32; i += 8) {
+        const int k = k0 + i;
+        const int64_t v = v0 + tx;
+        if (k < R && v < V) tile[i][tx] = A[(w * R + k) * V + v];
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int64_t v = v0 + i;
+        const int k = k0 + tx;
+        if (k < R && v < V) out[(w * V + v) * R + k] = tile[tx][i];
+    }
+}
+
 // Grid for warps walking (segment, 32-token slice) items: enough blocks for
 // the largest batch the batch info holds, at most eight per SM.
 int item_grid(const csgmv_batch_info &bi, int spp) {
@@ -296,6 +323,14 @@ cudaError_t launch_embedding(const EmbeddingParams &p, const csgmv_batch_info &b
                                        (const int32_t *)bi.lora_ranks, (const int32_t *)bi.num_segments_dev,
                                        (int32_t *)bi.status);
     if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_embedding(const uint16_t *A, int64_t L, int R, int64_t V, uint16_t *out,
+                                       cudaStream_t stream) {
+    if (L <= 0 || R <= 0 || V <= 0) return cudaSuccess;
+    const dim3 grid((unsigned)((V + 31) / 32), (unsigned)((R + 31) / 32), (unsigned)L);
+    transpose_embedding_kernel<<<grid, 256, 0, stream>>>(A, R, V, out);
     return cudaGetLastError();
 }
 

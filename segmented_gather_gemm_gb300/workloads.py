@@ -99,6 +99,7 @@ class EmbeddingWorkload:
     R: int
     max_chunk_size: int = 128
     chunk_override: int = 0
+    transposed: bool = False      # the table is passed as (L, V, R) (embedding_lora_a_transposed)
 
     @property
     def s(self) -> int:

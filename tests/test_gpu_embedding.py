@@ -148,3 +148,43 @@ def test_token_major_and_segment_kernels_agree():
     ref, bad = oracle.embedding_extra(ids, e.A_emb, extra, ta, e.ranks)
     assert bad == 0
     assert np.array_equal(outs[0], ref) and np.array_equal(outs[1], ref)
+
+
+def test_transpose_embedding_bit_exact():
+    e = wl.embedding_gather(seed=31, n_req=2, req_len=8, V=1000, R=40, L=3)
+    At = B.csgmv_transpose_embedding(dev_bf16(e.A_emb))
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(At), np.ascontiguousarray(e.A_emb.transpose(0, 2, 1)))
+
+
+@pytest.mark.parametrize("with_req", [True, False], ids=["token-major", "segments"])
+def test_transposed_layout_matches_oracle(with_req):
+    """The (L, V, R) table gives the oracle's bits on the (L, R, V) one, with
+    extra tokens, ragged and zero ranks and bad ids; and the full-size
+    workload bit-exact."""
+    e = wl.embedding_gather(seed=32, n_req=7, req_len=45, V=2000, R=24, L=4)
+    e.req_lens = np.array([45, 0, 100, 3, 45, 1, 17], np.int32)
+    e.ids = np.random.default_rng(6).integers(0, 2000, size=e.s).astype(np.int32)
+    e.ranks[:] = [24, 0, 7, 23]
+    ids, extra = _with_extra(e, 5, 0.2, 8)
+    ids[[3, 50]] = [2005, -1]
+    lens, ad = dev_i32(e.req_lens), dev_i32(e.req_adapter)
+    bi = B.BatchInfo.for_batch(len(e.req_lens), e.s, e.L, e.R, with_request_fields=with_req)
+    B.csgmv_build_batch_info(bi, lens, ad, e.s, dev_i32(e.ranks), dev_f32(np.ones(e.L, np.float32)))
+    At = B.csgmv_transpose_embedding(dev_bf16(e.A_emb))
+    out = torch.full((e.s, e.R), 5.0, dtype=torch.bfloat16, device="cuda")
+    B.embedding_lora_a_transposed(dev_i32(ids), At, e.V, dev_bf16(extra), out, bi)
+    torch.cuda.synchronize()
+    assert bi.device_status() & 4
+    ta = oracle.token_adapter(e.req_lens, e.req_adapter)
+    ref, bad = oracle.embedding_extra(ids, e.A_emb, extra, ta, e.ranks)
+    assert bad == 2 and np.array_equal(host_bits(out), ref)
+
+    f = wl.embedding_gather()
+    bi = build_batch(f)
+    At = B.csgmv_transpose_embedding(dev_bf16(f.A_emb))
+    out = torch.full((f.s, f.R), 5.0, dtype=torch.bfloat16, device="cuda")
+    B.embedding_lora_a_transposed(dev_i32(f.ids), At, f.V, None, out, bi)
+    torch.cuda.synchronize()
+    ref, bad = oracle.embedding(f.ids, f.A_emb, oracle.token_adapter(f.req_lens, f.req_adapter), f.ranks)
+    assert bad == 0 and np.array_equal(host_bits(out), ref)
