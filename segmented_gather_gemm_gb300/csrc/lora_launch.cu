@@ -458,7 +458,14 @@ cudaError_t launch_lora_sshrink(LoraParams &p, const csgmv_batch_info &bi, cudaS
                         CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && encode_2d(&k.tmXg, p.x, (uint64_t)p.K, (uint64_t)s, (uint64_t)p.K * 2, 64, 1,
                          CU_TENSOR_MAP_SWIZZLE_128B);
+    for (int i = 0; i < 4; ++i)
+        ok = ok && encode_2d(&k.tmXp[i], p.x, (uint64_t)p.K, (uint64_t)s, (uint64_t)p.K * 2, 64, 64u >> i,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && encode_2d(&k.tmA, p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2, 64, 16,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && encode_2d(&k.tmA32, p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2, 64, 32,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && encode_2d(&k.tmA64, p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2, 64, 64,
                          CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return cudaErrorInvalidValue;
 

@@ -113,7 +113,12 @@ __device__ void sh_producer(const ShrinkParams &k, unsigned char *smem, const in
             return t >= 0 ? t : tfill;
         };
         const int n16 = (p.c * r + 15) / 16;  // 16-row boxes of A: rows [0, round16(c*r)) of the slot
-        const uint32_t bytes = 128 * 128 + (uint32_t)n16 * 16 * 128;
+        // a partial tile's x rows as one box of 64, 32, 16 or 8 rows (the
+        // rest of the 128-row operand is stale and only feeds unused rows)
+        const int xb = T.M > 64 ? -1 : (T.M > 32 ? 0 : (T.M > 16 ? 1 : (T.M > 8 ? 2 : 3)));
+        const CUtensorMap *xmap = xb < 0 ? &k.tmX : &k.tmXp[xb];
+        const uint32_t xbytes = contig ? (xb < 0 ? 128u : 64u >> xb) * 128u : 128u * 128u;
+        const uint32_t bytes = xbytes + (uint32_t)n16 * 16 * 128;
         for (int ci = c0; ci < c1; ++ci, ++it) {
             const int s = it % k.S;
             mbar_wait(&W.empty[s], ((it / k.S) & 1) ^ 1, p.status, kStatusTimeout);
@@ -121,9 +126,14 @@ __device__ void sh_producer(const ShrinkParams &k, unsigned char *smem, const in
             const int k0 = ci * 64;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&W.full[s], bytes);
-                for (int i = 0; i < n16; ++i)
-                    tma_load_2d(st + 128 * 128 + i * 16 * 128, &k.tmA, k0, T.w * cR + 16 * i, &W.full[s]);
-                if (contig) tma_load_2d(st, &k.tmX, k0, t0, &W.full[s]);
+                // A rows [0, 16 * n16) as boxes of 64, then 32, then 16 rows
+                for (int i = 0; i < n16;) {
+                    const int nb = n16 - i >= 4 ? 4 : (n16 - i >= 2 ? 2 : 1);
+                    const CUtensorMap *am = nb == 4 ? &k.tmA64 : (nb == 2 ? &k.tmA32 : &k.tmA);
+                    tma_load_2d(st + 128 * 128 + i * 16 * 128, am, k0, T.w * cR + 16 * i, &W.full[s]);
+                    i += nb;
+                }
+                if (contig) tma_load_2d(st, xmap, k0, t0, &W.full[s]);
             }
             if (!contig) {
                 // lane l: tile rows 4l .. 4l+3 in one gather; rows past the tile
@@ -262,7 +272,10 @@ __global__ void __launch_bounds__(kShThreads, 1) lora_stream_shrink_kernel(const
         fence_mbar_init();
         prefetch_tmap(&k.tmX);
         prefetch_tmap(&k.tmXg);
+        for (int i = 0; i < 4; ++i) prefetch_tmap(&k.tmXp[i]);
         prefetch_tmap(&k.tmA);
+        prefetch_tmap(&k.tmA32);
+        prefetch_tmap(&k.tmA64);
     }
     if (warp == 1) {  // one warp owns the TMEM accumulators of the CTA
         tmem_alloc(W.tmem_slot, 2 * kShAccCols);

@@ -130,7 +130,9 @@ constexpr int kShEpiWarp0 = 2;
 struct ShrinkParams {
     CUtensorMap tmX;   // x (s rows, K): box 64 x 128, 128-byte swizzle
     CUtensorMap tmXg;  // the same, box 64 x 1 (4-row gathers)
+    CUtensorMap tmXp[4];  // the same, boxes of 64, 32, 16 and 8 rows (partial tiles: one box, little overfetch)
     CUtensorMap tmA;   // A (L * c * R rows, K): box 64 x 16, 128-byte swizzle
+    CUtensorMap tmA32, tmA64;  // the same, boxes of 32 and 64 rows (fewer TMA instructions per stage)
     LoraParams p;
     int runcap, max_segments;
     int max_parts;     // parts of K the output holds (1: h itself)
