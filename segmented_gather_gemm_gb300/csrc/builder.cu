@@ -49,6 +49,63 @@ __device__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
     return prefix;
 }
 
+// Exclusive block-wide scans of three values at once (one set of barriers
+// for all three); block totals in t[0..2].  `ws` is 3 * kWarps ints.
+__device__ void block_exclusive_scan3(const int (&v)[3], int (&pre)[3], int (&t)[3], int *ws) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc[3] = {v[0], v[1], v[2]};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+            const int n = __shfl_up_sync(0xffffffffu, inc[c], o);
+            if (lane >= o) inc[c] += n;
+        }
+    }
+    if (lane == 31)
+#pragma unroll
+        for (int c = 0; c < 3; ++c) ws[c * kWarps + warp] = inc[c];
+    __syncthreads();
+    if (warp < 3) {
+        int w = ws[warp * kWarps + lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += n;
+        }
+        ws[warp * kWarps + lane] = w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        pre[c] = (warp > 0 ? ws[c * kWarps + warp - 1] : 0) + inc[c] - v[c];
+        t[c] = ws[c * kWarps + kWarps - 1];
+    }
+    __syncthreads();
+}
+
+// For this lane: the sum of l over the lanes below it that carry the same
+// key, and (last) whether no lane above it does.  Lanes with equal keys are
+// found with one match; their lengths are read from `lens` (32 ints of
+// shared memory for this warp), so the cost follows the group size rather
+// than the warp width.  Every lane of the warp calls it.
+__device__ __forceinline__ int same_key_prefix(int key, int l, int *lens, bool &last) {
+    const int lane = threadIdx.x & 31;
+    lens[lane] = l;
+    __syncwarp();
+    const unsigned m = __match_any_sync(0xffffffffu, key);
+    const unsigned above = lane == 31 ? 0u : (0xffffffffu << (lane + 1));
+    last = (m & above) == 0u;
+    unsigned below = m & ((1u << lane) - 1u);
+    int pre = 0;
+    while (below) {
+        pre += lens[__ffs(below) - 1];
+        below &= below - 1u;
+    }
+    __syncwarp();
+    return pre;
+}
+
 // Largest i in [0, n) with a[i] <= key (a non-decreasing, a[0] <= key).
 __device__ int last_not_greater(const int *a, int n, int key) {
     int lo = 0, hi = n;  // answer in [lo, hi)
@@ -80,6 +137,9 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
     const int lane = tid & 31, warp = tid >> 5;
     const int chunk = p.chunk;
     int *wsum = flags + 2;  // [kWarps][L] per-warp token totals of each slot
+    int *tilebase = wsum + kWarps * L;  // [L] first decode tile of slot a
+    int *ws3 = tilebase + L;            // [3][kWarps] scan scratch
+    int *lens_w = ws3 + 3 * kWarps + 32 * warp;  // [kWarps][32] request lengths of each warp
     // Up to 1024 requests (one per thread) take one pass: each thread loads its
     // request once and keeps it in registers for the counts, the offsets and
     // its destination.
@@ -117,14 +177,8 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
             else if (my_l < 0) atomicOr(&flags[0], CSGMV_STATUS_BAD_LENS);
             else atomicAdd(&cnt[my_a], my_l);
         }
-        bool last = true;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const int ak = __shfl_sync(0xffffffffu, my_a, k);
-            const int lk = __shfl_sync(0xffffffffu, my_l, k);
-            if (ak == my_a && k < lane) my_pre += lk;
-            if (ak == my_a && k > lane) last = false;
-        }
+        bool last;
+        my_pre = same_key_prefix(my_a, my_l, lens_w, last);
         if (valid && last && my_a >= 0 && my_a < L) wsum[warp * L + my_a] = my_pre + my_l;
     } else {
         for (int i = tid; i < p.bs; i += kBuildThreads) {
@@ -158,22 +212,24 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
     }
     __syncthreads();
 
-    // Sorted-order base of each slot and its first segment.
-    int tcarry = 0, scarry = 0;
+    // Sorted-order base of each slot, its first segment and its first decode
+    // tile (csgmv_batch_info.tile_table: ceil(n / kDecTM) tiles per slot).
+    int tcarry = 0, scarry = 0, dcarry = 0;
     for (int a0 = 0; a0 < L; a0 += kBuildThreads) {
         int a = a0 + tid;
-        int n = (a < L) ? cnt[a] : 0;
-        int ns = (n + chunk - 1) / chunk;
-        int tt, st;
-        int tpre = block_exclusive_scan(n, warp_sums, &tt);
-        int spre = block_exclusive_scan(ns, warp_sums, &st);
+        const int n = (a < L) ? cnt[a] : 0;
+        const int v[3] = {n, (n + chunk - 1) / chunk, (n + kDecTM - 1) / kDecTM};
+        int pre[3], tot[3];
+        block_exclusive_scan3(v, pre, tot, ws3);
         if (a < L) {
-            tokbase[a] = tcarry + tpre;
-            run[a] = tcarry + tpre;
-            segbase[a] = scarry + spre;
+            tokbase[a] = tcarry + pre[0];
+            run[a] = tcarry + pre[0];
+            segbase[a] = scarry + pre[1];
+            tilebase[a] = dcarry + pre[2];
         }
-        tcarry += tt;
-        scarry += st;
+        tcarry += tot[0];
+        scarry += tot[1];
+        dcarry += tot[2];
     }
     if (tid == 0) {
         segbase[L] = scarry;
@@ -225,15 +281,8 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
             bool valid = i < p.bs;
             int a = valid ? p.req_adapter[i] : -1;
             int l = valid ? p.req_lens[i] : 0;
-            int pre = 0;
-            bool last = true;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                int ak = __shfl_sync(0xffffffffu, a, k);
-                int lk = __shfl_sync(0xffffffffu, l, k);
-                if (ak == a && k < lane) pre += lk;
-                if (ak == a && k > lane) last = false;
-            }
+            bool last;
+            const int pre = same_key_prefix(a, l, lens_w, last);
             for (int x = tid; x < kWarps * L; x += kBuildThreads) wsum[x] = 0;
             __syncthreads();
             if (valid && last) wsum[warp * L + a] = pre + l;
@@ -263,41 +312,30 @@ build_batch_info_kernel(BuildParams p, csgmv_batch_info bi) {
         }
     }
 
-    // permutation[dest of token t] = t.
-    for (int t = tid; t < p.num_tokens; t += kBuildThreads) {
-        int i = last_not_greater(req_start, p.bs + 1, t);
-        bi.permutation[req_dest[i] + (t - req_start[i])] = t;
+    // permutation[dest of token t] = t: one warp per request, whose tokens
+    // stay consecutive in sorted order.
+    for (int i = warp; i < p.bs; i += kWarps) {
+        const int s0 = req_start[i], n = req_start[i + 1] - s0, d0 = req_dest[i];
+        for (int j = lane; j < n; j += 32) bi.permutation[d0 + j] = s0 + j;
     }
 
     // Decode tiles (csgmv_batch_info.tile_table): slots in ascending order are
     // the slot runs; slot a's cnt[a] tokens become ceil(cnt[a] / kDecTM)
-    // tiles of balanced size.  The running positions in run[] are no longer
-    // needed: it takes the first tile of each slot.
+    // tiles of balanced size.
     if (bi.tile_table) {
-        __syncthreads();  // every thread is past its last use of run[]
-        int tcarry = 0;
-        for (int a0 = 0; a0 < L; a0 += kBuildThreads) {
-            const int a = a0 + tid;
-            const int nt = a < L ? (cnt[a] + kDecTM - 1) / kDecTM : 0;
-            int tot;
-            const int pre = block_exclusive_scan(nt, warp_sums, &tot);
-            if (a < L) run[a] = tcarry + pre;
-            tcarry += tot;
-        }
-        __syncthreads();
         int *rec = bi.tile_table + 4;
-        for (int t = tid; t < tcarry; t += kBuildThreads) {
-            const int a = last_not_greater(run, L, t);  // the last slot whose tiles start at or before t
+        for (int t = tid; t < dcarry; t += kBuildThreads) {
+            const int a = last_not_greater(tilebase, L, t);  // the last slot whose tiles start at or before t
             const int n = cnt[a];
             const int nt = (n + kDecTM - 1) / kDecTM;
-            const int i = t - run[a];
+            const int i = t - tilebase[a];
             const int lo = i * n / nt, hi = (i + 1) * n / nt;
             rec[4 * t] = a;
             rec[4 * t + 1] = tokbase[a] + lo;
             rec[4 * t + 2] = hi - lo;
             rec[4 * t + 3] = 0;
         }
-        if (tid < 4) bi.tile_table[tid] = tid == 0 ? tcarry : 0;
+        if (tid < 4) bi.tile_table[tid] = tid == 0 ? dcarry : 0;
     }
 
     // Per-request fields (chunked_backend.py _build_req_seg_indptr, req_weight_indices).
@@ -489,7 +527,8 @@ cudaError_t launch_build_lm_head(const BuildParams &p, const csgmv_batch_info &b
 }
 
 size_t build_smem_bytes(int bs, int max_loras) {
-    return sizeof(int) * ((size_t)4 * max_loras + 1 + 2 * (size_t)bs + 1 + kWarps + 2 + (size_t)kWarps * max_loras);
+    return sizeof(int) * ((size_t)5 * max_loras + 1 + 2 * (size_t)bs + 1 + kWarps + 2 + (size_t)kWarps * max_loras +
+                          3 * kWarps + 32 * kWarps);
 }
 
 cudaError_t launch_build(const BuildParams &p, const csgmv_batch_info &bi, cudaStream_t stream) {
