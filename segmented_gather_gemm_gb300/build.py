@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libcsgmv.so")
 SOURCES = ["api.cu", "builder.cu", "embedding.cu", "lora_launch.cu", "lora_fused.cu", "lora_shrink.cu", "lora_expand.cu",
-           "lora_small.cu", "lora_stream.cu", "lora_sshrink.cu", "lora_decode.cu",
+           "lora_small.cu", "lora_stream.cu", "lora_sshrink.cu", "lora_decode.cu", "lora_wide.cu",
            "qkv_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

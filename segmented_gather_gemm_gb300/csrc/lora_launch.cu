@@ -9,6 +9,7 @@
 
 #include "lora_decode.cuh"
 #include "lora_small.cuh"
+#include "lora_wide.cuh"
 #include "lora_stream.cuh"
 
 namespace csgmv {
@@ -20,6 +21,7 @@ const void *lora_kernel_small(int mode, int tm, int rmax);
 const void *lora_kernel_stream();
 const void *lora_kernel_sshrink();
 const void *lora_kernel_decode(int which, int rmax);
+const void *lora_kernel_wide(int tm, int rmax);
 
 namespace {
 
@@ -577,6 +579,80 @@ cudaError_t launch_lora_stream(LoraParams &p, const csgmv_batch_info &bi, cudaSt
     return cudaGetLastError();
 }
 
+// Slot runs of at most 8 tokens on average.
+bool wide_runs(const LoraParams &p, const csgmv_batch_info &bi) {
+    const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
+    return p.num_tokens / slots <= 8;
+}
+
+// Expand-only launch onto a wide output (a vocabulary-wide lm_head) on the
+// warp-specialized wide kernel (lora_wide.cuh).  Tiles of 32 tokens unless
+// slot runs average at most 8 tokens: a tile streams all of its slot's B
+// rows, so a slot of up to 32 tokens reads them once.
+cudaError_t launch_lora_wide(LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream, LaunchInfo *info) {
+    cudaError_t e = encoder();
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
+    const int tm = p.num_tokens / slots > 8 ? 32 : 16;
+    const int rmax = p.R <= 16 ? 16 : (p.R <= 32 ? 32 : 64);
+    const void *fn = lora_kernel_wide(tm, rmax);
+    if (!fn) return cudaErrorInvalidValue;
+    WideParams k;
+    memset(&k, 0, sizeof k);
+    k.p = p;
+    k.max_segments = bi.max_segments;
+    k.runcap = std::max(1, std::min(bi.max_segments, bi.max_loras + std::max(bi.max_bs, 1)));
+    const size_t budget = 227 * 1024;
+    const size_t fixed = align_up((size_t)(5 * k.runcap + 1 + 32) * 4 + 3 * 8 * 8, 1024) + 1024;
+    // 512-column stages when four of them fit, else 256
+    for (int nt = 512; nt >= 256; nt -= 256) {
+        k.nt = nt;
+        k.ypitch = nt * 2 + 16;
+        k.b_off = (int)align_up((size_t)tm * k.ypitch, 1024);
+        k.stage_bytes = (int)align_up((size_t)k.b_off + (size_t)nt * p.R * 2, 1024);
+        k.S = (int)std::min<size_t>(8, budget > fixed ? (budget - fixed) / k.stage_bytes : 0);
+        if (k.S >= 4) break;
+    }
+    if (k.S < 2) return cudaErrorInvalidConfiguration;
+    k.o_bar = 0;
+    k.o_run = (int)align_up((size_t)3 * k.S * 8, 16);
+    k.o_ring = (int)align_up((size_t)k.o_run + (size_t)(5 * k.runcap + 1 + 32) * 4, 1024);
+    const size_t smem = (size_t)k.o_ring + (size_t)k.S * k.stage_bytes + 1024;
+    // columns per unit: about six units per SM over the expected tiles
+    const int64_t ncols = p.off[p.c] - p.off[0];
+    const int tiles_est = std::max(slots, (p.num_tokens + tm - 1) / tm);
+    int64_t cb = (int64_t)tiles_est * ncols / ((int64_t)6 * sms);
+    cb = std::max<int64_t>(k.nt, (cb + k.nt - 1) / k.nt * k.nt);
+    k.cb = (int)std::min<int64_t>(cb, (ncols + k.nt - 1) / k.nt * k.nt);
+    const int nblk = (int)((ncols + k.cb - 1) / k.cb);
+    const int tiles_ub = (p.num_tokens + tm - 1) / tm + std::min(std::max(bi.bs, 1), std::max(bi.max_loras, 1));
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, (int64_t)tiles_ub * nblk));
+    if (!encode_b_maps(&k.tmB, k.tmBs, p, bi.max_loras, 256)) return cudaErrorInvalidValue;
+    if ((e = ensure_attrs(fn, dev, 1)) != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    set_dependent_launch(&attr[0]);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kWideThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (info) {
+        info->tm = tm;
+        info->crmax = rmax;
+        info->cluster = 1;
+        info->grid = grid;
+        info->smem = smem;
+    }
+    void *args[1] = {&k};
+    if ((e = cudaLaunchKernelExC(&cfg, fn, args)) != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 // Token tile for a batch: 16 for one or two tokens per slot run, 32 for a few,
 // 128 for prefill.
 int token_tile(const LoraParams &p, const csgmv_batch_info &bi) {
@@ -765,6 +841,12 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
     // Expand-only calls on 128-token tiles stream base through the
     // warp-specialized tcgen05 expand.
     if (tm == 128 && p.R >= 16 && mode == kModeExpand) return launch_lora_stream(p, bi, stream, info);
+    // Expand-only calls of very short slot runs (at most 8 tokens a slot on
+    // average, e.g. a pruned lm_head pass) onto a vocabulary-wide output: the
+    // warp-specialized wide kernel.  Longer runs measure faster on the
+    // small-tile kernel's 512-column stages.
+    if (mode == kModeExpand && tm <= 32 && p.off[p.c] - p.off[0] >= kWideCols && wide_runs(p, bi))
+        return launch_lora_wide(p, bi, stream, info);
     if (tm <= 32) {
         const cudaError_t es = launch_lora_small(mode, p, bi, stream, info, rmax, tm);
         if (es != cudaErrorInvalidConfiguration) return es;

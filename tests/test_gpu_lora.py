@@ -69,10 +69,11 @@ def test_fused_with_workspace_matches_oracle(case):
 WIDE = [
     (12, 40, 1, 256, [33024], 32, 6),
     (13, 24, 3, 136, [16384, 16400], 8, 5),
+    (14, 30, 2, 128, [16384, 8192, 8256], 64, 8),  # at most 8 tokens a slot: the wide kernel
 ]
 
 
-@pytest.mark.parametrize("case", WIDE, ids=["c1r32", "c2r8"])
+@pytest.mark.parametrize("case", WIDE, ids=["c1r32", "c2r8", "c3r64"])
 def test_wide_output_split_matches_oracle(case):
     """Vocabulary-wide outputs on small tiles take the two-kernel path: the
     oracle's result, with and without base, and bit-identical output with NaN
@@ -85,6 +86,31 @@ def test_wide_output_split_matches_oracle(case):
     y0, _ = run_fused(w, workspace=True)
     y1, _ = run_fused(make(*case, pad=float("nan"), min_len=1), workspace=True)
     assert np.array_equal(y0, y1), f"padding leaked into the output ({case})"
+
+
+@pytest.mark.parametrize("h_f32", [True, False])
+@pytest.mark.parametrize("slices", [[33024], [16392, 16392]], ids=["one-slice", "slice-edge-mid-pair"])
+def test_wide_expand_only(slices, h_f32):
+    """csgmv_expand onto a vocabulary-wide output with short slot runs (the
+    wide kernel): accumulate on and off (rank-0 slots then write zeros),
+    ragged ranks, fp32 and bf16 h, and a slice edge inside a 16-column pair."""
+    w = make(15, 40, 1, 64, slices, 32, 6, min_len=1)
+    bi = build_batch(w)
+    x, A, Bm = dev_bf16(w.x), dev_bf16(w.A), dev_bf16(w.B)
+    cR = w.c * w.R
+    h = torch.zeros((w.s, cR), dtype=torch.float32 if h_f32 else torch.bfloat16, device="cuda")
+    B.csgmv_shrink(x, A, w.c, h, bi)
+    torch.cuda.synchronize()
+    ta = oracle.token_adapter(w.req_lens, w.req_adapter)
+    hg = host_f64(h)
+    widest = int(np.max(np.diff(w.offsets)))
+    for acc in (True, False):
+        out = dev_bf16(w.base) if acc else torch.full((w.s, w.N), 3.0, dtype=torch.bfloat16, device="cuda")
+        B.csgmv_expand(h, Bm, w.offsets, w.c, widest, out, acc, bi)
+        torch.cuda.synchronize()
+        assert bi.device_status() == 0
+        yref = oracle.expand(hg, w.B, w.offsets, w.c, ta, w.ranks, w.scalings, w.base if acc else None)
+        assert_close(f64(host_bits(out)), yref, f"wide expand accumulate={acc}")
 
 
 def test_tiny_single_slice_workload():
