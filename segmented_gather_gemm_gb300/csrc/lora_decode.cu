@@ -366,6 +366,28 @@ __global__ void __launch_bounds__(kDecThreads, 2) lora_decode_shrink_kernel(cons
 }
 
 // ------------------------------------------------------------------------------------ expand
+// Column parts of one tile: slice j's 64-column blocks (counted from off[j])
+// go to cum[j + 1] - cum[j] parts, about Q * (its blocks) / (all blocks) and
+// at least enough for bmax blocks a part, so that no unit spans two slices.
+// cum[c] is the tile's unit count.
+__device__ __forceinline__ void dec_col_parts(const LoraParams &p, int Q, int bmax, int (&cum)[kMaxSlices + 1]) {
+    int b[kMaxSlices], B = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxSlices; ++j) {
+        b[j] = j < p.c ? (p.off[j + 1] - p.off[j] + 63) / 64 : 0;
+        B += b[j];
+    }
+    cum[0] = 0;
+    int acc = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxSlices; ++j) {
+        acc += b[j];
+        const int want = B > 0 ? (int)(((int64_t)Q * acc + B / 2) / B) : 0;
+        const int parts = b[j] > 0 ? max((b[j] + bmax - 1) / bmax, max(1, want - cum[j])) : 0;
+        cum[j + 1] = cum[j] + parts;
+    }
+}
+
 // Slice of output column col (slice offsets are multiples of 8, so an n8
 // column tile lies in one slice).
 __device__ __forceinline__ int slice_of(const LoraParams &p, int col) {
@@ -405,7 +427,10 @@ __global__ void __launch_bounds__(kDecExpThreads, 2) lora_decode_expand_kernel(c
     const int nblk = (ncols + 63) / 64;
     const int bmax = k.cols_max / 64;
     const int qmin = (nblk + bmax - 1) / bmax;
-    const int Q = max(qmin, min(nblk, ntiles > 0 ? (int)gridDim.x / ntiles : 1));
+    const int Qw = max(qmin, min(nblk, ntiles > 0 ? (int)gridDim.x / ntiles : 1));
+    int cum[kMaxSlices + 1];
+    dec_col_parts(p, Qw, bmax, cum);
+    const int Q = cum[p.c];  // units per tile
     const int units = ntiles * Q;
     const int my_row = dec_row_of_thread<kDecExpWarps>(lane, warp);
     const int pcB = p.R / 8, shB = pc_shift_of(pcB);
@@ -420,8 +445,11 @@ __global__ void __launch_bounds__(kDecExpThreads, 2) lora_decode_expand_kernel(c
         dec_tile(k, T, nruns, tile, w, p0, M);
         const int r = dec_rank(k, T, w, false);  // the shrink reports bad slots and ranks
         if (r <= 0 || M <= 0) continue;          // accumulate: rank 0 leaves y as it is
-        const int n0 = p.off[0] + 64 * (q * nblk / Q);
-        const int n1 = min(p.off[p.c], p.off[0] + 64 * ((q + 1) * nblk / Q));
+        int js = 0;
+        while (js + 1 < p.c && q >= cum[js + 1]) ++js;
+        const int bj = (p.off[js + 1] - p.off[js] + 63) / 64, parts = cum[js + 1] - cum[js], iq = q - cum[js];
+        const int n0 = p.off[js] + 64 * (iq * bj / parts);
+        const int n1 = min(p.off[js + 1], p.off[js] + 64 * ((iq + 1) * bj / parts));
         if (n1 <= n0) continue;
         const int nu = n1 - n0;
         const int nbox = (nu + 63) / 64;
@@ -533,7 +561,7 @@ __global__ void __launch_bounds__(kDecExpThreads, 2) lora_decode_expand_kernel(c
         // warp `warp` takes 16-column pairs warp, warp + 8, ...: per 16-row
         // tile, the pair's B fragments (ldmatrix x4, both n8 halves), h
         // fragments of each half's slice, hi and lo MMAs, then
-        // y = base + sigma * acc in place in the staged rows
+        // y = base + sigma * acc stored from registers
         const float sigma = T.sc[w];
         const int npairs = (nu + 15) / 16;
         const uint32_t hf_lane = hf_u + (uint32_t)lane * 16;
@@ -588,28 +616,24 @@ __global__ void __launch_bounds__(kDecExpThreads, 2) lora_decode_expand_kernel(c
                         }
                     }
                 }
+                // y = base + sigma * acc, stored from registers (a quad of
+                // lanes writes 16 consecutive bytes of a row)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (h == 1 && !has1) continue;
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int row = mt * 16 + (lane >> 2) + 8 * rr;
+                    if (row >= M) continue;
+                    const int t = T.perm[p0 + row];
+                    if (t < 0 || t >= p.num_tokens) continue;
 #pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        const int row = mt * 16 + (lane >> 2) + 8 * rr;
-                        if (row >= M) continue;
-                        const uint32_t a = ys_u + (uint32_t)(row * k.ypitch + (lc + 8 * h + 2 * (lane & 3)) * 2);
-                        const float2 bv = unpack_bf16x2(lds_b32(a));
-                        sts_b32(a, pack_bf16x2(bv.x + sigma * acc[h][2 * rr], bv.y + sigma * acc[h][2 * rr + 1]));
+                    for (int h = 0; h < 2; ++h) {
+                        if (h == 1 && !has1) continue;
+                        const int col = lc + 8 * h + 2 * (lane & 3);
+                        const float2 bv = unpack_bf16x2(lds_b32(ys_u + (uint32_t)(row * k.ypitch + col * 2)));
+                        *reinterpret_cast<uint32_t *>(p.y + (int64_t)t * p.N + n0 + col) =
+                            pack_bf16x2(bv.x + sigma * acc[h][2 * rr], bv.y + sigma * acc[h][2 * rr + 1]);
                     }
                 }
             }
-        }
-        __syncthreads();  // every warp's columns are in the staged rows
-        const int n16 = nu / 8;
-        for (int m = warp; m < M; m += kDecExpWarps) {
-            const int t = T.perm[p0 + m];
-            if (t < 0 || t >= p.num_tokens) continue;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.y + (int64_t)t * p.N + n0);
-            const uint4 *src = reinterpret_cast<const uint4 *>(ys + m * k.ypitch);
-            for (int c16 = lane; c16 < n16; c16 += 32) dst[c16] = src[c16];
         }
     }
 }

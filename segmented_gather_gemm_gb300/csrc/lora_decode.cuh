@@ -15,12 +15,12 @@
 // token) and the slot's A rows (one 64-column TMA box per K chunk) land on
 // one mbarrier; mma.sync m16n8k16 with fp32 accumulators; the partial sums go
 // to plane `part` of the workspace, rows indexed by sorted position.
-// Expand: unit = (tile, block of output columns).  Launched as a programmatic
-// dependent of the shrink, it loads its base rows and B rows while the shrink
-// is still running, then waits for the shrink, sums the planes of the h
-// columns it needs in part order (deterministic) straight into mma A
-// fragments (h as a bf16 hi + lo pair), runs the MMAs per 16-column pair,
-// adds base in place and stores 16-byte pieces.
+// Expand: unit = (tile, block of output columns of one slice).  Launched as a
+// programmatic dependent of the shrink, it loads its base rows and B rows
+// while the shrink is still running, then waits for the shrink, sums the
+// planes of its slice's h columns in part order (deterministic) straight into
+// mma A fragments (h as a bf16 hi + lo pair), runs the MMAs per 16-column
+// pair and stores y = base + sigma h B^T from registers.
 // The inner loops are specialised on warp-uniform tile counts and address
 // shared memory through precomputed 32-bit offsets: with a handful of
 // tokens per tile, instruction issue, not memory, sets the pace of a warp.
