@@ -52,29 +52,56 @@ __device__ __forceinline__ int warp_inclusive_scan(int v) {
 // the segments with shuffles while the others wait.  Returns the tile count
 // and the run count (-1: tiles come from the builder's records); every
 // thread of the block calls it, and it ends with a block barrier.
+template <int NT>
 __device__ int dec_build(const DecodeParams &k, const DecTab &T, int *nruns_out) {
     const LoraParams &p = k.p;
     const int tid = threadIdx.x;
-    const int nseg_raw = *p.num_segments_dev;
     const int ms = min(k.max_segments, kDecSegCap);
-    const int nt = blockDim.x;
-    for (int s = tid; s <= ms; s += nt) {
-        T.ip[s] = p.seg_indptr[s];
-        if (s < ms) T.sw[s] = p.weight_indices[s];
-    }
     const int nl = min(p.max_loras, kDecLoraCap);
-    for (int a = tid; a < nl; a += nt) {
-        T.rk[a] = p.lora_ranks[a];
-        T.sc[a] = p.scalings[a];
-    }
     const int nperm = min(p.num_tokens, kDecPermCap);
-    for (int i = tid; i < nperm; i += nt) T.perm[i] = p.permutation[i];
-    int built = -1;
-    if (p.tile_table) {
-        built = p.tile_table[0];
-        const int nrec = 4 * min(k.tile_cap, kDecRecCap);
-        for (int i = tid; i < nrec; i += nt) T.rec[i] = p.tile_table[4 + i];
+    const int nrec = p.tile_table ? 4 * min(k.tile_cap, kDecRecCap) : 0;
+    // a fixed number of words per thread, all loaded into registers before
+    // the first of them is stored, so that the loads overlap
+    constexpr int NIP = (kDecSegCap + NT) / NT, NL = (kDecLoraCap + NT - 1) / NT;
+    constexpr int NP = (kDecPermCap + NT - 1) / NT, NR = (4 * kDecRecCap + NT - 1) / NT;
+    int vip[NIP], vsw[NIP], vrk[NL], vp[NP], vrec[NR];
+    float vsc[NL];
+    const int nseg_raw = *p.num_segments_dev;
+    const int built = p.tile_table ? p.tile_table[0] : -1;
+#pragma unroll
+    for (int i = 0; i < NIP; ++i) {
+        const int s = tid + i * NT;
+        vip[i] = s <= ms ? p.seg_indptr[s] : 0;
+        vsw[i] = s < ms ? p.weight_indices[s] : 0;
     }
+#pragma unroll
+    for (int i = 0; i < NL; ++i) {
+        const int a = tid + i * NT;
+        vrk[i] = a < nl ? p.lora_ranks[a] : 0;
+        vsc[i] = a < nl ? p.scalings[a] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < NP; ++i) vp[i] = tid + i * NT < nperm ? p.permutation[tid + i * NT] : 0;
+#pragma unroll
+    for (int i = 0; i < NR; ++i) vrec[i] = tid + i * NT < nrec ? p.tile_table[4 + tid + i * NT] : 0;
+#pragma unroll
+    for (int i = 0; i < NIP; ++i) {
+        const int s = tid + i * NT;
+        if (s <= ms) T.ip[s] = vip[i];
+        if (s < ms) T.sw[s] = vsw[i];
+    }
+#pragma unroll
+    for (int i = 0; i < NL; ++i)
+        if (tid + i * NT < nl) {
+            T.rk[tid + i * NT] = vrk[i];
+            T.sc[tid + i * NT] = vsc[i];
+        }
+#pragma unroll
+    for (int i = 0; i < NP; ++i)
+        if (tid + i * NT < nperm) T.perm[tid + i * NT] = vp[i];
+#pragma unroll
+    for (int i = 0; i < NR; ++i)
+        if (tid + i * NT < nrec) T.rec[tid + i * NT] = vrec[i];
     __syncthreads();
     if (built >= 0) {
         *nruns_out = -1;
@@ -275,7 +302,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) lora_decode_shrink_kernel(cons
     // the expand may launch now: every word it reads before its own wait is final
     griddep_launch_dependents();
     int nruns;
-    const int ntiles = dec_build(k, T, &nruns);
+    const int ntiles = dec_build<kDecThreads>(k, T, &nruns);
     const int P = dec_parts(k, ntiles);
     const int units = ntiles * P;  // <= kDecPermCap * kDecMaxParts
     const uint32_t abox = (uint32_t)k.a_rows * 128;
@@ -421,7 +448,7 @@ __global__ void __launch_bounds__(kDecExpThreads, 2) lora_decode_expand_kernel(c
     // call's expand included) are complete.  Only the planes come from the
     // shrink itself.
     int nruns;
-    const int ntiles = dec_build(k, T, &nruns);
+    const int ntiles = dec_build<kDecExpThreads>(k, T, &nruns);
     const int P = dec_parts(k, ntiles);
     const int ncols = p.off[p.c] - p.off[0];
     const int nblk = (ncols + 63) / 64;
