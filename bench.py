@@ -164,12 +164,12 @@ def load_peaks():
 
 
 # Sources of the kernels behind each recorded traffic figure, with their
-# launcher and shared headers: the small-tile kernel for decode and lm_head
-# shapes, the warp-specialized shrink and the tcgen05 expand for prefill.
+# launcher and shared headers: the decode kernels, the small-tile shrink and
+# the wide expand for lm_head, the streaming tcgen05 kernels for prefill.
 _SHARED_SOURCES = ("lora_tma.cuh", "lora_launch.cu", "device_utils.cuh", "csgmv_internal.h")
 KERNEL_SOURCES = {
     "decode_qkv": ("lora_decode.cuh", "lora_decode.cu") + _SHARED_SOURCES,
-    "lm_head_decode": ("lora_small.cuh", "lora_small.cu") + _SHARED_SOURCES,
+    "lm_head_decode": ("lora_small.cuh", "lora_small.cu", "lora_wide.cuh", "lora_wide.cu") + _SHARED_SOURCES,
     "prefill_gate_up": ("lora_stream.cuh", "lora_stream.cu", "lora_sshrink.cu") + _SHARED_SOURCES,
     "skewed_down_proj": ("lora_stream.cuh", "lora_stream.cu", "lora_sshrink.cu") + _SHARED_SOURCES,
 }

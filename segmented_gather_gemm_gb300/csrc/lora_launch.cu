@@ -579,16 +579,16 @@ cudaError_t launch_lora_stream(LoraParams &p, const csgmv_batch_info &bi, cudaSt
     return cudaGetLastError();
 }
 
-// Slot runs of at most 8 tokens on average.
+// Slot runs of at most 16 tokens on average.
 bool wide_runs(const LoraParams &p, const csgmv_batch_info &bi) {
     const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
-    return p.num_tokens / slots <= 8;
+    return p.num_tokens / slots <= 16;
 }
 
 // Expand-only launch onto a wide output (a vocabulary-wide lm_head) on the
-// warp-specialized wide kernel (lora_wide.cuh).  Tiles of 32 tokens unless
-// slot runs average at most 8 tokens: a tile streams all of its slot's B
-// rows, so a slot of up to 32 tokens reads them once.
+// warp-specialized wide kernel (lora_wide.cuh), on 16-token tiles (32-token
+// tiles need twice the accumulators and measured slower).  A tile streams all
+// of its slot's B rows, so a slot of up to 16 tokens reads them once.
 cudaError_t launch_lora_wide(LoraParams &p, const csgmv_batch_info &bi, cudaStream_t stream, LaunchInfo *info) {
     cudaError_t e = encoder();
     if (e != cudaSuccess) return e;
@@ -596,7 +596,7 @@ cudaError_t launch_lora_wide(LoraParams &p, const csgmv_batch_info &bi, cudaStre
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int slots = std::max(1, std::min(std::max(bi.bs, 1), bi.num_loras > 0 ? bi.num_loras : bi.max_loras));
-    const int tm = p.num_tokens / slots > 8 ? 32 : 16;
+    const int tm = 16;
     const int rmax = p.R <= 16 ? 16 : (p.R <= 32 ? 32 : 64);
     const void *fn = lora_kernel_wide(tm, rmax);
     if (!fn) return cudaErrorInvalidValue;
@@ -605,8 +605,15 @@ cudaError_t launch_lora_wide(LoraParams &p, const csgmv_batch_info &bi, cudaStre
     k.p = p;
     k.max_segments = bi.max_segments;
     k.runcap = std::max(1, std::min(bi.max_segments, bi.max_loras + std::max(bi.max_bs, 1)));
+    // tiles by slot when the grouped table fits its share of shared memory
+    k.nslot = std::max(1, p.max_loras);
+    k.segcap = std::max(1, bi.max_segments);
+    k.tokcap = std::max(1, p.num_tokens);
+    k.grouped = wide_group_ints(k.nslot, k.segcap, k.tokcap) * 4 <= (size_t)kWideGroupBytes;
+    const size_t table_ints = std::max<size_t>((size_t)5 * k.runcap + 1 + 32,
+                                               k.grouped ? wide_group_ints(k.nslot, k.segcap, k.tokcap) : 0);
     const size_t budget = 227 * 1024;
-    const size_t fixed = align_up((size_t)(5 * k.runcap + 1 + 32) * 4 + 3 * 8 * 8, 1024) + 1024;
+    const size_t fixed = align_up(table_ints * 4 + 3 * 8 * 8, 1024) + 1024;
     // 512-column stages when four of them fit, else 256
     for (int nt = 512; nt >= 256; nt -= 256) {
         k.nt = nt;
@@ -619,7 +626,7 @@ cudaError_t launch_lora_wide(LoraParams &p, const csgmv_batch_info &bi, cudaStre
     if (k.S < 2) return cudaErrorInvalidConfiguration;
     k.o_bar = 0;
     k.o_run = (int)align_up((size_t)3 * k.S * 8, 16);
-    k.o_ring = (int)align_up((size_t)k.o_run + (size_t)(5 * k.runcap + 1 + 32) * 4, 1024);
+    k.o_ring = (int)align_up((size_t)k.o_run + table_ints * 4, 1024);
     const size_t smem = (size_t)k.o_ring + (size_t)k.S * k.stage_bytes + 1024;
     // columns per unit: about six units per SM over the expected tiles
     const int64_t ncols = p.off[p.c] - p.off[0];
@@ -841,10 +848,10 @@ cudaError_t launch_lora(int mode, LoraParams &p, const csgmv_batch_info &bi, cud
     // Expand-only calls on 128-token tiles stream base through the
     // warp-specialized tcgen05 expand.
     if (tm == 128 && p.R >= 16 && mode == kModeExpand) return launch_lora_stream(p, bi, stream, info);
-    // Expand-only calls of very short slot runs (at most 8 tokens a slot on
-    // average, e.g. a pruned lm_head pass) onto a vocabulary-wide output: the
-    // warp-specialized wide kernel.  Longer runs measure faster on the
-    // small-tile kernel's 512-column stages.
+    // Expand-only calls of short slot runs (at most 16 tokens a slot on
+    // average: an lm_head decode or pruned lm_head pass) onto a
+    // vocabulary-wide output: the warp-specialized wide kernel.  Longer runs
+    // take the small-tile kernel's 512-column stages.
     if (mode == kModeExpand && tm <= 32 && p.off[p.c] - p.off[0] >= kWideCols && wide_runs(p, bi))
         return launch_lora_wide(p, bi, stream, info);
     if (tm <= 32) {

@@ -13,6 +13,11 @@
 //            y = base + sigma h B^T stored straight from registers (a quad
 //            of lanes writes 16 consecutive bytes of a row), after which
 //            they free the slot.
+// Tiles group a slot's tokens wherever its segments lie (a pruned lm_head
+// batch keeps its requests in request order, so one slot's tokens are spread
+// over several segments): every token of slot w goes to w's tiles, so B rows
+// of a slot are read once per TM of its tokens.  Rows of a tile need no
+// order, since every output row depends on its own h row alone.
 // No barrier spans the CTA inside the stream: each stage has a full barrier
 // (the copies' bytes) and an empty barrier (the consumer warps).  A stage of
 // a short tile is little arithmetic but a long chain of dependent
@@ -27,6 +32,12 @@
 namespace csgmv {
 
 constexpr int kWideConsumers = 16;
+constexpr int kWideGroupBytes = 32 * 1024;  // shared memory a grouped tile table may take
+
+// Ints of a grouped tile table (lora_wide.cu wide_group).
+inline size_t wide_group_ints(int nslot, int segcap, int tokcap) {
+    return (size_t)5 * nslot + 3 + 4 * (size_t)segcap + tokcap + 32;
+}
 constexpr int kWideWarps = 2 + kWideConsumers;  // load, one spare, consumers
 constexpr int kWideThreads = kWideWarps * 32;
 
@@ -35,6 +46,10 @@ struct WideParams {
     CUtensorMap tmBs[kMaxSlices];  // B per slice tensor (p.b_tuple): box R x 64
     LoraParams p;
     int runcap, max_segments;
+    int grouped;      // tiles by slot (nslot, segcap, tokcap below); else tiles of segment runs
+    int nslot;        // slots the grouped table counts (max_loras)
+    int segcap;       // segments it holds (max_segments)
+    int tokcap;       // positions it holds (num_tokens)
     int nt;           // columns per stage (256 or 512)
     int cb;           // columns per unit (a multiple of nt)
     int S;            // ring stages

@@ -110,3 +110,33 @@ def test_lm_head_delta_over_pruned_rows():
     ta = np.repeat(adapter, lens).astype(np.int32)
     ref = oracle.fused(x, w.A, w.B, [0, N], 1, ta, ranks, scal, base)
     assert_close(host_f64(y), ref, "lm_head pruned rows")
+
+
+def test_lm_head_vocabulary_wide_grouped_tiles():
+    """The pruned rows of a vocabulary-wide lm_head through csgmv_qkv with a
+    workspace: the expand groups each slot's tokens from segments spread over
+    the whole batch (request order), some slots holding more than one 16-token
+    tile; every output row against the oracle, and rows of zero-length
+    requests absent."""
+    rng = np.random.default_rng(23)
+    bs, L, R, K, N = 200, 32, 32, 256, 33024
+    lens = rng.integers(0, 4, size=bs).astype(np.int32)
+    adapter = rng.integers(0, L, size=bs).astype(np.int32)
+    adapter[:40] = 3  # one slot with well over 16 tokens in many segments
+    w = wl.random_lora(29, bs=4, max_len=8, K=K, N_slices=[N], R=R, L=L)
+    ranks, scal = w.ranks, w.scalings
+    s = int(lens.sum())
+    x = wl.normal_bf16(rng, (s, K), 0.5)
+    base = wl.normal_bf16(rng, (s, N), 0.5)
+    bi = lm_build(lens, adapter, ranks, scal, R=R)
+    assert bi.device_status() == 0
+    ws = torch.empty(B.csgmv_qkv_workspace_bytes(bi, 1) // 4, dtype=torch.float32, device="cuda")
+    assert B.csgmv_qkv_path(bi, K, N, [0, N], 1, ws.numel() * 4) == "small_split"
+    y = dev_bf16(base)
+    B.csgmv_qkv(dev_bf16(x), dev_bf16(w.A), dev_bf16(w.B), [0, N], 1, N, y, bi, workspace=ws)
+    torch.cuda.synchronize()
+    assert bi.device_status() == 0
+    ta = np.repeat(adapter, lens).astype(np.int32)
+    assert np.sum(ta == 3) > 32
+    ref = oracle.fused(x, w.A, w.B, [0, N], 1, ta, ranks, scal, base)
+    assert_close(host_f64(y), ref, "vocabulary-wide lm_head rows")

@@ -66,14 +66,17 @@ def test_fused_with_workspace_matches_oracle(case):
 # (seed, bs, max_len, K, slices, R, L): short requests on a handful of slots and
 # at least 32768 output columns, so that csgmv_qkv with a workspace runs the
 # 16-token shrink into the workspace and then the expand-only launch
+# (at most 16 tokens a slot on average: the wide kernel; more: the small-tile
+# kernel's expand-only launch)
 WIDE = [
     (12, 40, 1, 256, [33024], 32, 6),
     (13, 24, 3, 136, [16384, 16400], 8, 5),
-    (14, 30, 2, 128, [16384, 8192, 8256], 64, 8),  # at most 8 tokens a slot: the wide kernel
+    (14, 30, 2, 128, [16384, 8192, 8256], 64, 8),
+    (16, 40, 4, 128, [33024], 16, 3),  # about 30 tokens a slot: the small-tile expand
 ]
 
 
-@pytest.mark.parametrize("case", WIDE, ids=["c1r32", "c2r8", "c3r64"])
+@pytest.mark.parametrize("case", WIDE, ids=["c1r32", "c2r8", "c3r64", "c1r16-small"])
 def test_wide_output_split_matches_oracle(case):
     """Vocabulary-wide outputs on small tiles take the two-kernel path: the
     oracle's result, with and without base, and bit-identical output with NaN
