@@ -613,7 +613,8 @@ cudaError_t launch_lora_wide(LoraParams &p, const csgmv_batch_info &bi, cudaStre
     const size_t table_ints = std::max<size_t>((size_t)5 * k.runcap + 1 + 32,
                                                k.grouped ? wide_group_ints(k.nslot, k.segcap, k.tokcap) : 0);
     const size_t budget = 227 * 1024;
-    const size_t fixed = align_up(table_ints * 4 + 3 * 8 * 8, 1024) + 1024;
+    const size_t hf_bytes = (size_t)2 * kWideHfInts * 4 + 2 * 32 * 4;  // h fragments and tokens, two buffers
+    const size_t fixed = align_up(3 * 8 * 8 + 32 + table_ints * 4 + 16 + hf_bytes, 1024) + 1024;
     // 512-column stages when four of them fit, else 256
     for (int nt = 512; nt >= 256; nt -= 256) {
         k.nt = nt;
@@ -625,8 +626,10 @@ cudaError_t launch_lora_wide(LoraParams &p, const csgmv_batch_info &bi, cudaStre
     }
     if (k.S < 2) return cudaErrorInvalidConfiguration;
     k.o_bar = 0;
-    k.o_run = (int)align_up((size_t)3 * k.S * 8, 16);
-    k.o_ring = (int)align_up((size_t)k.o_run + table_ints * 4, 1024);
+    k.o_hbar = (int)align_up((size_t)3 * k.S * 8, 16);
+    k.o_run = (int)align_up((size_t)k.o_hbar + 4 * 8, 16);
+    k.o_hf = (int)align_up((size_t)k.o_run + table_ints * 4, 16);
+    k.o_ring = (int)align_up((size_t)k.o_hf + hf_bytes, 1024);
     const size_t smem = (size_t)k.o_ring + (size_t)k.S * k.stage_bytes + 1024;
     // columns per unit: about six units per SM over the expected tiles
     const int64_t ncols = p.off[p.c] - p.off[0];

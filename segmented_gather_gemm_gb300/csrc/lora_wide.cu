@@ -226,19 +226,66 @@ __device__ void wide_load(const WideParams &k, unsigned char *smem, const int *t
     }
 }
 
-// --------------------------------------------------------------------------------------- consume
-// h[t][col] summed over the workspace planes (one plane: h itself).
-__device__ __forceinline__ float wide_h(const LoraParams &p, int t, int col) {
-    float v = 0.f;
-    const int parts = max(1, p.h_parts);
-    for (int q = 0; q < parts; ++q) {
-        const int64_t o = (int64_t)q * p.h_plane + (int64_t)t * p.ldh + col;
-        v += p.h_f32 ? reinterpret_cast<const float *>(p.h)[o]
-                     : __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.h)[o]);
+// ----------------------------------------------------------------------------------------- h prep
+// The spare warp, for one-slice outputs: per unit (the consumers' order) the
+// tokens of its TM = 16 rows and the h fragments every consumer lane holds
+// (lane L: rows L / 4 and L / 4 + 8, columns 2 (L % 4) + {0, 1, 8, 9} of each
+// k16 step, planes summed in part order), as bf16 hi / lo pairs, into buffer
+// it % 2 once the consumers have taken what it held before.
+template <int TM, int RMAX>
+__device__ void wide_hprep(const WideParams &k, unsigned char *smem, const int *tables, int nruns, int nblk,
+                           int units) {
+    constexpr int KS = RMAX / 16;
+    static_assert(TM == 16, "one 16-row tile per unit");
+    const LoraParams &p = k.p;
+    const int lane = threadIdx.x & 31;
+    uint64_t *hfull = reinterpret_cast<uint64_t *>(smem + k.o_hbar), *hempty = hfull + 2;
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        WUnit U;
+        if (!wide_unit<TM>(k, tables, nruns, nblk, u, false, U)) continue;
+        const int b = it & 1;
+        mbar_wait(&hempty[b], ((it >> 1) & 1) ^ 1, p.status, kStatusTimeout);
+        uint32_t *hf = reinterpret_cast<uint32_t *>(smem + k.o_hf) + b * kWideHfInts;
+        int *tok = reinterpret_cast<int *>(smem + k.o_hf) + 2 * kWideHfInts + b * 32;
+        const int t = lane < TM ? wide_token(k, tables, nruns, U, lane) : -1;
+        tok[lane] = t;
+        const int tA = __shfl_sync(0xffffffffu, t, lane >> 2), tB = __shfl_sync(0xffffffffu, t, (lane >> 2) + 8);
+        float v[KS][8];
+        const int parts = max(1, p.h_parts);
+#pragma unroll
+        for (int q = 0; q < kMaxKParts; ++q) {
+            if (q > 0 && q >= parts) break;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int kk = ks * 16 + 2 * (lane & 3) + (e & 1) + ((e & 4) ? 8 : 0);
+                    const int tt = (e & 2) ? tB : tA;
+                    float x = 0.f;
+                    if (kk < U.r && tt >= 0) {
+                        const int64_t o = (int64_t)q * p.h_plane + (int64_t)tt * p.ldh + kk;
+                        x = p.h_f32 ? reinterpret_cast<const float *>(p.h)[o]
+                                    : __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.h)[o]);
+                    }
+                    v[ks][e] = q == 0 ? x : v[ks][e] + x;
+                }
+        }
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int rg = 0; rg < 4; ++rg) {
+                uint32_t hi, lo;
+                split_pair(v[ks][2 * rg], v[ks][2 * rg + 1], hi, lo);
+                hf[((ks * 2 + 0) * 4 + rg) * 32 + lane] = hi;
+                hf[((ks * 2 + 1) * 4 + rg) * 32 + lane] = lo;
+            }
+        mbar_arrive(&hfull[b]);  // every lane: its own writes are released
+        ++it;
     }
-    return v;
 }
 
+// --------------------------------------------------------------------------------------- consume
 // NT8 = n8 tiles per consumer warp and stage (k.nt / kWideConsumers / 8).
 // In the one-slice path the warp's n8 tile j, row n holds stage column
 // lc0 + 2 * NT8 * (n / 2) + 2 * j + n % 2: the accumulator layout of
@@ -273,35 +320,71 @@ __device__ void wide_consume(const WideParams &k, unsigned char *smem, const int
                 boff[qq][ks] = (uint32_t)swz(row, 2 * ks + ((lane >> 3) & 1), pcB, shB) * 2u;
             }
         }
-    uint32_t it = 0;
+    // the spare warp prepares h for one-slice outputs (TM = 16 only)
+    const bool hprep = TM == 16 && p.c == 1;
+    uint64_t *hfull = reinterpret_cast<uint64_t *>(smem + k.o_hbar), *hempty = hfull + 2;
+    uint32_t it = 0, hit = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
         WUnit U;
         if (!wide_unit<TM>(k, tables, nruns, nblk, u, false, U)) continue;
         const float sigma = U.r > 0 ? p.scalings[U.w] : 0.f;
         const int ksteps = (U.r + 15) / 16;
         const bool r_ragged = U.r > 0 && (p.R == 8 ? (U.r < 8) : (U.r % 16 != 0));
-        // tokens of the rows this lane's fragments hold: mt * 16 + lane / 4 (+ 8)
+        // tokens of the rows this lane's fragments hold: mt * 16 + lane / 4 (+ 8),
+        // and h of one slice as bf16 hi / lo A fragments, every 16-row tile
         int trow[NMT][2];
-#pragma unroll
-        for (int mt = 0; mt < NMT; ++mt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) trow[mt][hh] = wide_token(k, tables, nruns, U, mt * 16 + (lane >> 2) + 8 * hh);
-        // h of one slice as bf16 hi / lo A fragments, every 16-row tile
         uint32_t fhi[NMT][KS][4], flo[NMT][KS][4];
         int cur = -1;
-        auto load_slice = [&](int j) {
-            // every value is loaded before any is split, so the loads overlap
-            float v[NMT][KS][8];
+        if (hprep) {  // one slice, 16-row tiles: from the spare warp
+            const int b = hit & 1;
+            mbar_wait(&hfull[b], (hit >> 1) & 1, p.status, kStatusTimeout);
+            const uint32_t *hf = reinterpret_cast<const uint32_t *>(smem + k.o_hf) + b * kWideHfInts;
+            const int *tok = reinterpret_cast<const int *>(smem + k.o_hf) + 2 * kWideHfInts + b * 32;
+            trow[0][0] = tok[lane >> 2];
+            trow[0][1] = tok[(lane >> 2) + 8];
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int rg = 0; rg < 4; ++rg) {
+                    fhi[0][ks][rg] = hf[((ks * 2 + 0) * 4 + rg) * 32 + lane];
+                    flo[0][ks][rg] = hf[((ks * 2 + 1) * 4 + rg) * 32 + lane];
+                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&hempty[b]);
+            ++hit;
+            cur = 0;
+        } else {
 #pragma unroll
             for (int mt = 0; mt < NMT; ++mt)
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks)
+                for (int hh = 0; hh < 2; ++hh)
+                    trow[mt][hh] = wide_token(k, tables, nruns, U, mt * 16 + (lane >> 2) + 8 * hh);
+        }
+        auto load_slice = [&](int j) {
+            // plane 0 of every value first (all loads in flight at once),
+            // then the further planes in part order
+            float v[NMT][KS][8];
+            const int parts = max(1, p.h_parts);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int kk = ks * 16 + 2 * (lane & 3) + (e & 1) + ((e & 4) ? 8 : 0);
-                        const int t = trow[mt][(e >> 1) & 1];
-                        v[mt][ks][e] = kk < U.r && t >= 0 ? wide_h(p, t, j * U.r + kk) : 0.f;
-                    }
+            for (int q = 0; q < kMaxKParts; ++q) {
+                if (q > 0 && q >= parts) break;
+#pragma unroll
+                for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int kk = ks * 16 + 2 * (lane & 3) + (e & 1) + ((e & 4) ? 8 : 0);
+                            const int t = trow[mt][(e >> 1) & 1];
+                            float x = 0.f;
+                            if (kk < U.r && t >= 0) {
+                                const int64_t o = (int64_t)q * p.h_plane + (int64_t)t * p.ldh + j * U.r + kk;
+                                x = p.h_f32 ? reinterpret_cast<const float *>(p.h)[o]
+                                            : __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(p.h)[o]);
+                            }
+                            v[mt][ks][e] = q == 0 ? x : v[mt][ks][e] + x;
+                        }
+            }
 #pragma unroll
             for (int mt = 0; mt < NMT; ++mt)
 #pragma unroll
@@ -506,6 +589,11 @@ __global__ void __launch_bounds__(kWideThreads, 1) lora_wide_expand_kernel(const
             mbar_init(&W.done[i], kWideConsumers);
             mbar_init(&W.empty[i], kWideConsumers);
         }
+        uint64_t *hb = reinterpret_cast<uint64_t *>(smem + k.o_hbar);
+        mbar_init(&hb[0], 32);  // hfull: every lane of the h warp
+        mbar_init(&hb[1], 32);
+        mbar_init(&hb[2], kWideConsumers);  // hempty: one lane per consumer warp
+        mbar_init(&hb[3], kWideConsumers);
         fence_mbar_init();
         prefetch_tmap(&k.tmB);
         if (k.p.b_tuple)
@@ -526,6 +614,9 @@ __global__ void __launch_bounds__(kWideThreads, 1) lora_wide_expand_kernel(const
     const int nblk = (ncols + k.cb - 1) / k.cb;
     const int units = ntiles * nblk;
     if (warp == 0) wide_load<TM>(k, smem, tables, nruns, nblk, units);
+    else if (warp == 1) {
+        if (TM == 16 && k.p.c == 1) wide_hprep<TM, RMAX>(k, smem, tables, nruns, nblk, units);
+    }
     else if (warp >= 2) {
         if (k.nt == 512) wide_consume<TM, RMAX, 4>(k, smem, tables, nruns, nblk, units, warp - 2);
         else wide_consume<TM, RMAX, 2>(k, smem, tables, nruns, nblk, units, warp - 2);
