@@ -407,7 +407,9 @@ size_t carve_sshrink(ShrinkParams &k, int S) {
         return (int)o;
     };
     k.S = S;
-    k.stage_bytes = (int)align_up((size_t)128 * 128 + align_up((size_t)k.p.c * k.p.R, 16) * 128, 1024);
+    k.a_off = kShChunks * 128 * 128;
+    k.a_bytes = (int)(align_up((size_t)k.p.c * k.p.R, 16) * 128);
+    k.stage_bytes = (int)align_up((size_t)k.a_off + (size_t)kShChunks * k.a_bytes, 1024);
     k.o_bar = take((size_t)(2 * S + 6) * 8 + 16, 16);
     k.o_run = take((size_t)(8 * k.runcap + 1 + 32) * 4, 16);  // run table cut at token gaps
     k.o_tok = take((size_t)(2 * 128 + 2) * 4, 16);

@@ -119,28 +119,33 @@ __device__ void sh_producer(const ShrinkParams &k, unsigned char *smem, const in
         const CUtensorMap *xmap = xb < 0 ? &k.tmX : &k.tmXp[xb];
         const uint32_t xbytes = contig ? (xb < 0 ? 128u : 64u >> xb) * 128u : 128u * 128u;
         const uint32_t bytes = xbytes + (uint32_t)n16 * 16 * 128;
-        for (int ci = c0; ci < c1; ++ci, ++it) {
+        for (int ci = c0; ci < c1; ci += kShChunks, ++it) {
             const int s = it % k.S;
+            const int nch = min(kShChunks, c1 - ci);  // chunks in this stage
             mbar_wait(&W.empty[s], ((it / k.S) & 1) ^ 1, p.status, kStatusTimeout);
             unsigned char *st = smem + k.o_ring + s * k.stage_bytes;
-            const int k0 = ci * 64;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&W.full[s], bytes);
-                // A rows [0, 16 * n16) as boxes of 64, then 32, then 16 rows
-                for (int i = 0; i < n16;) {
-                    const int nb = n16 - i >= 4 ? 4 : (n16 - i >= 2 ? 2 : 1);
-                    const CUtensorMap *am = nb == 4 ? &k.tmA64 : (nb == 2 ? &k.tmA32 : &k.tmA);
-                    tma_load_2d(st + 128 * 128 + i * 16 * 128, am, k0, T.w * cR + 16 * i, &W.full[s]);
-                    i += nb;
-                }
-                if (contig) tma_load_2d(st, xmap, k0, t0, &W.full[s]);
+                mbar_arrive_expect_tx(&W.full[s], bytes * (uint32_t)nch);
+                if (contig)
+                    for (int j = 0; j < nch; ++j) tma_load_2d(st + j * 128 * 128, xmap, (ci + j) * 64, t0, &W.full[s]);
+                // A rows [0, 16 * n16) of each chunk as boxes of 64, then 32, then 16 rows
+                for (int j = 0; j < nch; ++j)
+                    for (int i = 0; i < n16;) {
+                        const int nb = n16 - i >= 4 ? 4 : (n16 - i >= 2 ? 2 : 1);
+                        const CUtensorMap *am = nb == 4 ? &k.tmA64 : (nb == 2 ? &k.tmA32 : &k.tmA);
+                        tma_load_2d(st + k.a_off + j * k.a_bytes + i * 16 * 128, am, (ci + j) * 64, T.w * cR + 16 * i,
+                                    &W.full[s]);
+                        i += nb;
+                    }
             }
             if (!contig) {
                 // lane l: tile rows 4l .. 4l+3 in one gather; rows past the tile
                 // (or of an invalid token) read a valid row that is never used
                 __syncwarp();  // after the byte count is posted
                 const int m = 4 * lane;
-                tma_gather4(st + m * 128, &k.tmXg, k0, grow(m), grow(m + 1), grow(m + 2), grow(m + 3), &W.full[s]);
+                for (int j = 0; j < nch; ++j)
+                    tma_gather4(st + j * 128 * 128 + m * 128, &k.tmXg, (ci + j) * 64, grow(m), grow(m + 1), grow(m + 2),
+                                grow(m + 3), &W.full[s]);
             }
         }
         ++uc;
@@ -163,17 +168,21 @@ __device__ void sh_mma(const ShrinkParams &k, unsigned char *smem, const int *ta
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32(128, (p.c * r + 15) & ~15);
         const uint32_t d = tmem + (uint32_t)(b * kShAccCols);
-        for (int ci = c0; ci < c1; ++ci, ++it) {
+        for (int ci = c0; ci < c1; ci += kShChunks, ++it) {
             const int s = it % k.S;
+            const int nch = min(kShChunks, c1 - ci);
             mbar_wait(&W.full[s], (it / k.S) & 1, p.status, kStatusTimeout);
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t xa = smem_u32(smem + k.o_ring + s * k.stage_bytes);
-                const uint32_t aa = xa + 128 * 128;
+                const uint32_t sa = smem_u32(smem + k.o_ring + s * k.stage_bytes);
+                for (int j = 0; j < nch; ++j) {
+                    const uint32_t xa = sa + j * 128 * 128;
+                    const uint32_t aa = sa + k.a_off + j * k.a_bytes;
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    tc_mma_bf16(d, smem_desc_kmajor(xa + ks * 32, 128), smem_desc_kmajor(aa + ks * 32, 128), idesc,
-                                ci > c0 || ks > 0);
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc_mma_bf16(d, smem_desc_kmajor(xa + ks * 32, 128), smem_desc_kmajor(aa + ks * 32, 128), idesc,
+                                    ci > c0 || j > 0 || ks > 0);
+                }
                 tc_commit(&W.empty[s]);
             }
             __syncwarp();
