@@ -173,13 +173,22 @@ __device__ void st_mma(const StreamParams &k, unsigned char *smem, const int *ta
             mbar_wait(&W.b_full[sb], (g / k.Sb) & 1, p.status, kStatusTimeout);
             unsigned char *bs = smem + k.o_bring + sb * k.b_slot_bytes;
             if (RK != r) {  // B columns [r, RK) are adapter padding (even NaN): zero them
-                const int c0 = r >> 3, nc = (RK >> 3) - c0;
-                for (int idx = lane; idx < kStCols * nc; idx += 32) {
-                    const int n = idx / nc, ch = c0 + idx % nc;
-                    uint16_t *q16 = reinterpret_cast<uint16_t *>(bs) + swz(n, ch, pcB, shB);
+                // lane l takes rows l and l + 32: whole padding chunks as one
+                // 16-byte store, a chunk holding column r element by element
+                const int cpart = r >> 3, nc = (RK >> 3) - cpart;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        if (ch * 8 + e >= r) q16[e] = 0;
+                for (int h2 = 0; h2 < kStCols / 32; ++h2) {
+                    const int n = lane + 32 * h2;
+                    for (int ch = cpart; ch < cpart + nc; ++ch) {
+                        uint16_t *q16 = reinterpret_cast<uint16_t *>(bs) + swz(n, ch, pcB, shB);
+                        if (ch * 8 >= r) {
+                            *reinterpret_cast<uint4 *>(q16) = make_uint4(0u, 0u, 0u, 0u);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                if (ch * 8 + e >= r) q16[e] = 0;
+                        }
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
