@@ -388,7 +388,7 @@ size_t carve_stream(StreamParams &k, int Sy) {
     k.Sb = kStBSlots;
     k.y_slot_bytes = kStBoxes * kStTileBytes;
     k.b_slot_bytes = kStCols * k.p.R * 2;
-    k.o_bar = take((size_t)(2 * k.Sb + 2 * Sy + 2 * kStAcc + 4) * 8 + 16, 16);
+    k.o_bar = take((size_t)(3 * k.Sb + 2 * Sy + 2 * kStAcc + 4) * 8 + 16 + (size_t)k.Sb * 4, 16);
     k.o_run = take((size_t)(8 * k.runcap + 1 + 32) * 4, 16);  // run table cut at token gaps
     k.o_tok = take((size_t)(2 * 128 + 8) * 4, 16);
     k.o_bring = take((size_t)k.Sb * k.b_slot_bytes, 1024);

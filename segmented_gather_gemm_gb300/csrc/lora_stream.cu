@@ -8,6 +8,8 @@ constexpr int kStOpBar = 1;              // named barrier of the operand warps
 
 struct StBars {
     uint64_t *b_full, *b_empty;      // [Sb]
+    uint64_t *b_ready;               // [Sb] B tile landed and its padding columns zeroed
+    int *bpad;                       // [Sb] rank r | round16(r) << 16 of the tile in each B slot
     uint64_t *y_full, *y_empty;      // [Sy]
     uint64_t *acc_full, *acc_empty;  // [kStAcc]
     uint64_t *op_full, *op_empty;    // [2]
@@ -27,7 +29,9 @@ __device__ __forceinline__ StBars st_bars(const StreamParams &k, unsigned char *
     w.acc_empty = w.acc_full + kStAcc;
     w.op_full = w.acc_empty + kStAcc;
     w.op_empty = w.op_full + 2;
-    w.tmem_slot = reinterpret_cast<uint32_t *>(w.op_empty + 2);
+    w.b_ready = w.op_empty + 2;
+    w.tmem_slot = reinterpret_cast<uint32_t *>(w.b_ready + k.Sb);
+    w.bpad = reinterpret_cast<int *>(w.tmem_slot + 4);
     w.tok = reinterpret_cast<int *>(smem + k.o_tok);
     w.flag = w.tok + 256;
     return w;
@@ -65,13 +69,50 @@ __device__ __forceinline__ bool st_unit(const StreamParams &k, const int *tables
 
 // ------------------------------------------------------------------------------------- producers
 // B tiles: they need no token list, so this warp runs ahead of the operand
-// tiles by as many stages as the B ring holds.
+// tiles by as many stages as the B ring holds.  A tile of a slot whose rank r
+// is not a multiple of 16 carries adapter padding in columns [r, round16(r))
+// (even NaN), which must be zero before its MMAs: this warp zeroes it D
+// stages after issuing the tile (waiting for it to land), then releases the
+// slot to the MMA warp (b_ready), so the padding pass is off the MMA warp's
+// per-stage chain.  D < Sb: the slot the producer waits to refill was
+// released D stages of issue earlier.
 __device__ void st_b_producer(const StreamParams &k, unsigned char *smem, const int *tables, int nruns,
                               int64_t nunits) {
     const LoraParams &p = k.p;
     const int lane = threadIdx.x & 31;
     const StBars W = st_bars(k, smem);
     const uint32_t Bbytes = (uint32_t)kStCols * p.R * 2;  // kStBoxes boxes of 64 B rows
+    const int pcB = p.R / 8, shB = pc_shift_of(pcB);
+    const uint32_t D = (uint32_t)max(1, k.Sb / 2);
+    auto release = [&](uint32_t gz) {
+        const int sb = gz % k.Sb;
+        mbar_wait(&W.b_full[sb], (gz / k.Sb) & 1, p.status, kStatusTimeout);
+        const int info = W.bpad[sb];
+        const int r = info & 0xffff, RK = info >> 16;
+        if (RK != r) {
+            // lane l takes rows l and l + 32: whole padding chunks as one
+            // 16-byte store, a chunk holding column r element by element
+            unsigned char *bs = smem + k.o_bring + sb * k.b_slot_bytes;
+            const int cpart = r >> 3, nc = (RK >> 3) - cpart;
+#pragma unroll
+            for (int h2 = 0; h2 < kStCols / 32; ++h2) {
+                const int n = lane + 32 * h2;
+                for (int ch = cpart; ch < cpart + nc; ++ch) {
+                    uint16_t *q16 = reinterpret_cast<uint16_t *>(bs) + swz(n, ch, pcB, shB);
+                    if (ch * 8 >= r) {
+                        *reinterpret_cast<uint4 *>(q16) = make_uint4(0u, 0u, 0u, 0u);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            if (ch * 8 + e >= r) q16[e] = 0;
+                    }
+                }
+            }
+            fence_proxy_async_smem();  // the tensor core reads these columns
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&W.b_ready[sb]);
+    };
     uint32_t g = 0;
     for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
         StUnit U;
@@ -85,14 +126,17 @@ __device__ void st_b_producer(const StreamParams &k, unsigned char *smem, const 
             mbar_wait(&W.b_empty[sb], ((g / k.Sb) & 1) ^ 1, p.status, kStatusTimeout);
             if (lane == 0) {
                 unsigned char *bs = smem + k.o_bring + sb * k.b_slot_bytes;
+                W.bpad[sb] = r | (((r + 15) & ~15) << 16);
                 mbar_arrive_expect_tx(&W.b_full[sb], Bbytes);
 #pragma unroll
                 for (int bx = 0; bx < kStBoxes; ++bx)
                     tma_load_2d(bs + bx * 64 * p.R * 2, &k.tmB[U.j], 0, brow + x0 + 64 * bx, &W.b_full[sb]);
             }
             __syncwarp();
+            if (g >= D) release(g - D);
         }
     }
+    for (uint32_t gz = g > D ? g - D : 0; gz < g; ++gz) release(gz);
 }
 
 // Base rows of every stage, through the tile's token list.
@@ -170,29 +214,9 @@ __device__ void st_mma(const StreamParams &k, unsigned char *smem, const int *ta
         for (int i = 0; i < U.nt; ++i, ++g) {
             const int sb = g % k.Sb;
             const int a = g % kStAcc;
-            mbar_wait(&W.b_full[sb], (g / k.Sb) & 1, p.status, kStatusTimeout);
+            // landed, padding columns [r, RK) zeroed by the B producer
+            mbar_wait(&W.b_ready[sb], (g / k.Sb) & 1, p.status, kStatusTimeout);
             unsigned char *bs = smem + k.o_bring + sb * k.b_slot_bytes;
-            if (RK != r) {  // B columns [r, RK) are adapter padding (even NaN): zero them
-                // lane l takes rows l and l + 32: whole padding chunks as one
-                // 16-byte store, a chunk holding column r element by element
-                const int cpart = r >> 3, nc = (RK >> 3) - cpart;
-#pragma unroll
-                for (int h2 = 0; h2 < kStCols / 32; ++h2) {
-                    const int n = lane + 32 * h2;
-                    for (int ch = cpart; ch < cpart + nc; ++ch) {
-                        uint16_t *q16 = reinterpret_cast<uint16_t *>(bs) + swz(n, ch, pcB, shB);
-                        if (ch * 8 >= r) {
-                            *reinterpret_cast<uint4 *>(q16) = make_uint4(0u, 0u, 0u, 0u);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                if (ch * 8 + e >= r) q16[e] = 0;
-                        }
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
             mbar_wait(&W.acc_empty[a], ((g / kStAcc) & 1) ^ 1, p.status, kStatusTimeout);
             tc_fence_after();
             if (lane == 0) {
@@ -420,6 +444,7 @@ __global__ void __launch_bounds__(kStThreads, 1) lora_stream_expand_kernel(const
         for (int i = 0; i < k.Sb; ++i) {
             mbar_init(&W.b_full[i], 1);
             mbar_init(&W.b_empty[i], 1);
+            mbar_init(&W.b_ready[i], 1);
         }
         for (int i = 0; i < k.Sy; ++i) {
             mbar_init(&W.y_full[i], 1);
