@@ -407,9 +407,9 @@ size_t carve_sshrink(ShrinkParams &k, int S) {
         return (int)o;
     };
     k.S = S;
-    k.a_off = kShChunks * 128 * 128;
+    k.a_off = k.chunks * 128 * 128;
     k.a_bytes = (int)(align_up((size_t)k.p.c * k.p.R, 16) * 128);
-    k.stage_bytes = (int)align_up((size_t)k.a_off + (size_t)kShChunks * k.a_bytes, 1024);
+    k.stage_bytes = (int)align_up((size_t)k.a_off + (size_t)k.chunks * k.a_bytes, 1024);
     k.o_bar = take((size_t)(2 * S + 6) * 8 + 16, 16);
     k.o_run = take((size_t)(8 * k.runcap + 1 + 32) * 4, 16);  // run table cut at token gaps
     k.o_tok = take((size_t)(2 * 128 + 2) * 4, 16);
@@ -436,9 +436,16 @@ cudaError_t launch_lora_sshrink(LoraParams &p, const csgmv_batch_info &bi, cudaS
     k.max_segments = bi.max_segments;
     k.runcap = std::max(1, std::min(bi.max_segments, bi.max_loras + std::max(bi.max_bs, 1)));
     const size_t budget = 227 * 1024;
+    // the most K chunks per stage that still leave three stages, else two
+    // chunks and as many stages as fit (up to eight)
     int S = 8;
-    size_t smem = carve_sshrink(k, S);
-    while (smem > budget && S > 2) smem = carve_sshrink(k, --S);
+    size_t smem = 0;
+    for (k.chunks = kShChunksMax; k.chunks >= 2; --k.chunks) {
+        S = 8;
+        smem = carve_sshrink(k, S);
+        while (smem > budget && S > 2) smem = carve_sshrink(k, --S);
+        if (smem <= budget && (S >= 3 || k.chunks == 2)) break;
+    }
     if (smem > budget) return cudaErrorInvalidConfiguration;
     e = ensure_attrs(fn, dev, 1);
     if (e != cudaSuccess) return e;

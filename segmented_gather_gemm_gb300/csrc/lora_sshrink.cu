@@ -119,9 +119,9 @@ __device__ void sh_producer(const ShrinkParams &k, unsigned char *smem, const in
         const CUtensorMap *xmap = xb < 0 ? &k.tmX : &k.tmXp[xb];
         const uint32_t xbytes = contig ? (xb < 0 ? 128u : 64u >> xb) * 128u : 128u * 128u;
         const uint32_t bytes = xbytes + (uint32_t)n16 * 16 * 128;
-        for (int ci = c0; ci < c1; ci += kShChunks, ++it) {
+        for (int ci = c0; ci < c1; ci += k.chunks, ++it) {
             const int s = it % k.S;
-            const int nch = min(kShChunks, c1 - ci);  // chunks in this stage
+            const int nch = min(k.chunks, c1 - ci);  // chunks in this stage
             mbar_wait(&W.empty[s], ((it / k.S) & 1) ^ 1, p.status, kStatusTimeout);
             unsigned char *st = smem + k.o_ring + s * k.stage_bytes;
             if (lane == 0) {
@@ -168,9 +168,9 @@ __device__ void sh_mma(const ShrinkParams &k, unsigned char *smem, const int *ta
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32(128, (p.c * r + 15) & ~15);
         const uint32_t d = tmem + (uint32_t)(b * kShAccCols);
-        for (int ci = c0; ci < c1; ci += kShChunks, ++it) {
+        for (int ci = c0; ci < c1; ci += k.chunks, ++it) {
             const int s = it % k.S;
-            const int nch = min(kShChunks, c1 - ci);
+            const int nch = min(k.chunks, c1 - ci);
             mbar_wait(&W.full[s], (it / k.S) & 1, p.status, kStatusTimeout);
             tc_fence_after();
             if (lane == 0) {

@@ -124,11 +124,13 @@ struct StreamParams {
 // writes h itself, with zeros in columns [c*r, c*R) and in rows of rank-0
 // tokens.
 constexpr int kShWarps = 6;
-// 64-column K chunks per ring stage: the x boxes of a stage are neighbouring
-// 128-byte pieces of each token row, which the DRAM serves far better asked
-// for together (a probe streaming x-shaped rows: 5.0 TB/s with one chunk per
-// request, 6.1 TB/s with two, for the same bytes in flight).
-constexpr int kShChunks = 2;
+// 64-column K chunks per ring stage (at most; the launcher takes three when
+// three stages of them fit, else two): the x boxes of a stage are
+// neighbouring 128-byte pieces of each token row, which the DRAM serves far
+// better asked for together (a probe streaming x-shaped rows: 5.0 TB/s with
+// one chunk per request, 6.1 TB/s with two, 6.6 TB/s with four, for the same
+// bytes in flight).
+constexpr int kShChunksMax = 3;
 constexpr int kShThreads = kShWarps * 32;
 constexpr int kShEpiWarp0 = 2;
 
@@ -144,8 +146,9 @@ struct ShrinkParams {
     int *parts_out;    // where the chosen part count goes (the workspace header), or NULL
     int S;             // ring stages
     int o_bar, o_run, o_tok, o_ring;
-    int stage_bytes;   // kShChunks x tiles, then kShChunks A tiles of round16(c * R) rows
-    int a_off;         // offset of the first A tile in a stage (kShChunks x tiles)
+    int chunks;        // K chunks per stage (1 .. kShChunksMax)
+    int stage_bytes;   // `chunks` x tiles, then `chunks` A tiles of round16(c * R) rows
+    int a_off;         // offset of the first A tile in a stage (`chunks` x tiles)
     int a_bytes;       // bytes of one A tile
     int64_t plane;     // elements of h between two parts (P > 1)
 };
