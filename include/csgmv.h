@@ -311,9 +311,12 @@ CSGMV_API size_t csgmv_qkv_workspace_bytes(const csgmv_batch_info *bi, int num_s
  * takes the same arguments without one and uses a fixed 32 MiB array in the
  * library's own device memory as the h workspace; the library allocates
  * nothing and frees nothing here either.
- *   - Limit: the batch's h, num_tokens * num_slices * max_rank * 4 bytes,
- *     and a 256-byte header must fit in 32 MiB, else CSGMV_ERR_CAPACITY
- *     (nothing is launched).
+ *   - Limit: when csgmv_qkv would take a two-kernel path, the batch's h,
+ *     num_tokens * num_slices * max_rank * 4 bytes, and a 256-byte header
+ *     must fit in 32 MiB, else CSGMV_ERR_CAPACITY (nothing is launched).  A
+ *     batch whose h does not fit but which csgmv_qkv runs as one kernel
+ *     (csgmv_qkv_path gives CSGMV_PATH_FUSED even with an unbounded
+ *     workspace) runs that way, with no workspace.
  *   - Every GPU that loads the library holds the 32 MiB until the process
  *     exits.
  *   - The first call on each device looks up the array's device address

@@ -1,6 +1,7 @@
 // csgmv_qkv for callers that cannot allocate device memory at call time (see
 // the declaration in csgmv.h): the h workspace of the two-kernel path is a
 // fixed array in the library's own device memory instead of a caller buffer.
+#include <cstdint>
 #include <cstdio>
 #include <mutex>
 
@@ -49,6 +50,12 @@ extern "C" CSGMV_API int csgmv_qkv_static_scratch(const void *x, int64_t K, cons
                                                (size_t)(num_slices > 0 ? num_slices : 0) *
                                                (size_t)(bi->max_rank > 0 ? bi->max_rank : 0) * 4;
     if (need > kStaticScratchFloats * 4) {
+        // a batch whose h does not fit may still take the one-kernel path,
+        // which needs no workspace at all
+        const int path = csgmv_qkv_path(bi, K, N, slice_offsets, num_slices, SIZE_MAX);
+        if (path == CSGMV_PATH_FUSED || path < 0)  // (errors: csgmv_qkv reports them)
+            return csgmv_qkv(x, K, A, B, N, slice_offsets, num_slices, max_slice_size, base_output, nullptr, 0, bi,
+                             stream);
         char msg[160];
         snprintf(msg, sizeof msg, "csgmv_qkv_static_scratch: h needs %zu bytes, the static scratch holds %zu",
                  need, kStaticScratchFloats * 4);

@@ -67,12 +67,36 @@ def test_static_scratch_matches_csgmv_qkv_on_two_calls_in_a_row(make):
 
 
 def test_static_scratch_rejects_a_batch_too_large_for_it():
-    # 50000 tokens x 3 slices x rank 64 x 4 bytes of h exceed the 32 MiB array;
-    # the call is refused before anything is launched
+    # 50000 tokens x 3 slices x rank 64 x 4 bytes of h exceed the 32 MiB array
+    # and the batch would take the two-kernel path: the call is refused before
+    # anything is launched
     bi = B.BatchInfo.for_batch(1, 50000, 1, 64)
     bi.c.num_tokens = 50000
     t = torch.zeros((8, 64), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((8, 192), dtype=torch.bfloat16, device="cuda")
+    assert B.csgmv_qkv_path(bi, 64, 192, [0, 64, 128, 192], 3, 1 << 40) == "stream"
     with pytest.raises(B.CsgmvError) as err:
-        B.csgmv_qkv_static_scratch(t, t, t, [0, 64, 128, 192], 3, 64, t, bi)
+        B.csgmv_qkv_static_scratch(t, t, t, [0, 64, 128, 192], 3, 64, y, bi)
     assert err.value.code == -2
     assert "static scratch" in str(err.value)
+
+
+def test_static_scratch_runs_a_one_kernel_batch_too_large_for_it():
+    """A batch whose h exceeds the 32 MiB array but which csgmv_qkv runs as one
+    kernel (128-token tiles with a rank-8 buffer, which the streaming kernels
+    do not take) is run, not refused: bit-identical to csgmv_qkv without a
+    workspace."""
+    w = wl.random_lora(41, bs=4, max_len=90000, K=64, N_slices=[16, 16, 16], R=8, L=4,
+                       rank_choices=[4, 8], zero_rank_prob=0.0, std=0.5, min_len=90000)
+    assert w.s * w.c * w.R * 4 + 256 > 32 * 1024 * 1024
+    bi = build_batch(w)
+    assert B.csgmv_qkv_path(bi, w.K, w.N, w.offsets, w.c, 1 << 40) == "fused"
+    x, A, Bm = dev_bf16(w.x), dev_bf16(w.A), dev_bf16(w.B)
+    widest = int(np.max(np.diff(w.offsets)))
+    ys = dev_bf16(w.base)
+    B.csgmv_qkv_static_scratch(x, A, Bm, w.offsets, w.c, widest, ys, bi)
+    yf = dev_bf16(w.base)
+    B.csgmv_qkv(x, A, Bm, w.offsets, w.c, widest, yf, bi)
+    torch.cuda.synchronize()
+    assert bi.device_status() == 0
+    assert torch.equal(ys, yf)
