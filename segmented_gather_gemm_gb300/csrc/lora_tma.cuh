@@ -262,28 +262,45 @@ __device__ int build_run_table_raw(const LoraParams &p, int max_segments, int ru
     // capacity rather than by the segment count (which is loaded alongside).
     const int cap = max_segments;
     const int nseg_raw = *p.num_segments_dev;
+    // each pass gives thread tid the G consecutive segments k0 + G*tid + j:
+    // every load of a pass goes out before the first is used, and one block
+    // scan numbers the runs of G * nt segments
+    constexpr int G = 4;
     int carry = 0;
-    for (int k0 = 0; k0 < cap; k0 += nt) {
-        const int s = k0 + tid;
-        int w_here = -1, w_prev = -1, ip0 = 0, ip1 = 0;
-        if (s < cap) {
-            w_here = p.weight_indices[s];
-            if (s > 0) w_prev = p.weight_indices[s - 1];
-            ip0 = p.seg_indptr[s];
-            ip1 = p.seg_indptr[s + 1];
+    for (int k0 = 0; k0 < cap; k0 += G * nt) {
+        const int s0 = k0 + G * tid;
+        int w[G + 2], ip[G + 1];  // w[j + 1] = weight_indices[s0 + j], j = -1 .. G; ip[j] = seg_indptr[s0 + j]
+#pragma unroll
+        for (int j = -1; j <= G; ++j) {
+            const int s = s0 + j;
+            w[j + 1] = s >= 0 && s < cap ? p.weight_indices[s] : -1;
+        }
+#pragma unroll
+        for (int j = 0; j <= G; ++j) {
+            const int s = s0 + j;
+            ip[j] = s <= cap ? p.seg_indptr[s] : 0;
         }
         const int nseg = max(0, min(nseg_raw, cap));
         if (k0 >= nseg) break;
-        const int st = s < nseg && (s == 0 || w_here != w_prev);
-        const int en = s < nseg && (s == nseg - 1 || p.weight_indices[min(s + 1, cap - 1)] != w_here);
-        int tot;
-        const int pre = block_scan(st, scratch, &tot);
-        const int run = carry + pre + st - 1;  // run of segment s
-        if (st && run < runcap) {
-            run_w[run] = w_here;
-            run_p0[run] = max(0, min(ip0, p.num_tokens));
+        int st[G], en[G], cnt = 0;
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            const int s = s0 + j;
+            st[j] = s < nseg && (s == 0 || w[j + 1] != w[j]);
+            en[j] = s < nseg && (s == nseg - 1 || w[j + 2] != w[j + 1]);
+            cnt += st[j];
         }
-        if (en && run >= 0 && run < runcap) run_len[run] = max(0, min(ip1, p.num_tokens));  // run end for now
+        int tot;
+        int run = carry + block_scan(cnt, scratch, &tot) - 1;  // run of the segment before s0
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            run += st[j];  // run of segment s0 + j
+            if (st[j] && run < runcap) {
+                run_w[run] = w[j + 1];
+                run_p0[run] = max(0, min(ip[j], p.num_tokens));
+            }
+            if (en[j] && run >= 0 && run < runcap) run_len[run] = max(0, min(ip[j + 1], p.num_tokens));  // run end for now
+        }
         carry += tot;
     }
     int nruns = carry;
