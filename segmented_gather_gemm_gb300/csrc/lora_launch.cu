@@ -57,6 +57,23 @@ bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
     return r == CUDA_SUCCESS;
 }
 
+// 3D bf16 view of a row-major (outer, inner) tensor as (64-column chunks,
+// rows, chunk index): dims {64, outer, inner / 64}, strides {row_bytes, 128},
+// box {64, box_rows, box_chunks}, 128-byte swizzle.  One load then fills
+// box_chunks tiles of box_rows x 64, one after the other.
+bool encode_3d_chunks(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                      uint32_t box_rows, uint32_t box_chunks) {
+    if (!g_encode || inner % 64 != 0 || box_rows > 256 || box_chunks > 256) return false;
+    cuuint64_t dims[3] = {64, outer, inner / 64};
+    cuuint64_t strides[2] = {row_bytes, 128};
+    cuuint32_t box[3] = {64, box_rows, box_chunks};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 CUtensorMapSwizzle swizzle_for_row_bytes(int bytes) {
     return bytes >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B
          : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -479,6 +496,11 @@ cudaError_t launch_lora_sshrink(LoraParams &p, const csgmv_batch_info &bi, cudaS
     ok = ok && encode_2d(&k.tmA64, p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2, 64, 64,
                          CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return cudaErrorInvalidValue;
+    // one-instruction stages when K splits into whole chunks (else the 2-D maps)
+    k.use3d = p.K % 64 == 0 &&
+              encode_3d_chunks(&k.tmX3, p.x, (uint64_t)p.K, (uint64_t)s, (uint64_t)p.K * 2, 128, k.chunks) &&
+              encode_3d_chunks(&k.tmA3, p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2,
+                               (uint32_t)k.a_bytes / 128, k.chunks);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);

@@ -118,25 +118,37 @@ __device__ void sh_producer(const ShrinkParams &k, unsigned char *smem, const in
         const int xb = T.M > 64 ? -1 : (T.M > 32 ? 0 : (T.M > 16 ? 1 : (T.M > 8 ? 2 : 3)));
         const CUtensorMap *xmap = xb < 0 ? &k.tmX : &k.tmXp[xb];
         const uint32_t xbytes = contig ? (xb < 0 ? 128u : 64u >> xb) * 128u : 128u * 128u;
-        const uint32_t bytes = xbytes + (uint32_t)n16 * 16 * 128;
         for (int ci = c0; ci < c1; ci += k.chunks, ++it) {
             const int s = it % k.S;
             const int nch = min(k.chunks, c1 - ci);  // chunks in this stage
+            // a whole stage of whole chunks: x (a full contiguous tile) and A
+            // each as one 3-D box over the stage's chunks; A then brings
+            // round16(c*R) rows (rows past the rank feed no output column)
+            const bool full3 = k.use3d && nch == k.chunks;
+            const bool x3 = full3 && contig && xb < 0;
+            const uint32_t sbytes = (uint32_t)nch * (xbytes + (full3 ? (uint32_t)k.a_bytes : (uint32_t)n16 * 16 * 128));
             mbar_wait(&W.empty[s], ((it / k.S) & 1) ^ 1, p.status, kStatusTimeout);
             unsigned char *st = smem + k.o_ring + s * k.stage_bytes;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&W.full[s], bytes * (uint32_t)nch);
-                if (contig)
+                mbar_arrive_expect_tx(&W.full[s], sbytes);
+                if (x3) {
+                    tma_load_3d(st, &k.tmX3, 0, t0, ci, &W.full[s]);
+                } else if (contig) {
                     for (int j = 0; j < nch; ++j) tma_load_2d(st + j * 128 * 128, xmap, (ci + j) * 64, t0, &W.full[s]);
-                // A rows [0, 16 * n16) of each chunk as boxes of 64, then 32, then 16 rows
-                for (int j = 0; j < nch; ++j)
-                    for (int i = 0; i < n16;) {
-                        const int nb = n16 - i >= 4 ? 4 : (n16 - i >= 2 ? 2 : 1);
-                        const CUtensorMap *am = nb == 4 ? &k.tmA64 : (nb == 2 ? &k.tmA32 : &k.tmA);
-                        tma_load_2d(st + k.a_off + j * k.a_bytes + i * 16 * 128, am, (ci + j) * 64, T.w * cR + 16 * i,
-                                    &W.full[s]);
-                        i += nb;
-                    }
+                }
+                if (full3) {
+                    tma_load_3d(st + k.a_off, &k.tmA3, 0, T.w * cR, ci, &W.full[s]);
+                } else {
+                    // A rows [0, 16 * n16) of each chunk as boxes of 64, then 32, then 16 rows
+                    for (int j = 0; j < nch; ++j)
+                        for (int i = 0; i < n16;) {
+                            const int nb = n16 - i >= 4 ? 4 : (n16 - i >= 2 ? 2 : 1);
+                            const CUtensorMap *am = nb == 4 ? &k.tmA64 : (nb == 2 ? &k.tmA32 : &k.tmA);
+                            tma_load_2d(st + k.a_off + j * k.a_bytes + i * 16 * 128, am, (ci + j) * 64, T.w * cR + 16 * i,
+                                        &W.full[s]);
+                            i += nb;
+                        }
+                }
             }
             if (!contig) {
                 // lane l: tile rows 4l .. 4l+3 in one gather; rows past the tile

@@ -140,6 +140,12 @@ struct ShrinkParams {
     CUtensorMap tmXp[4];  // the same, boxes of 64, 32, 16 and 8 rows (partial tiles: one box, little overfetch)
     CUtensorMap tmA;   // A (L * c * R rows, K): box 64 x 16, 128-byte swizzle
     CUtensorMap tmA32, tmA64;  // the same, boxes of 32 and 64 rows (fewer TMA instructions per stage)
+    // 3-D views (64 columns, rows, K chunks of 64) of x and A whose box holds
+    // a stage's `chunks` chunks in one instruction: x 128 rows, A round16(c*R)
+    // rows, written [chunk][row][128 B] like the per-chunk tiles (use3d: K is
+    // a multiple of 64 and both maps encoded)
+    CUtensorMap tmX3, tmA3;
+    int use3d;
     LoraParams p;
     int runcap, max_segments;
     int max_parts;     // parts of K the output holds (1: h itself)
