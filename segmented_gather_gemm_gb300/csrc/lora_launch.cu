@@ -501,6 +501,9 @@ cudaError_t launch_lora_sshrink(LoraParams &p, const csgmv_batch_info &bi, cudaS
               encode_3d_chunks(&k.tmX3, p.x, (uint64_t)p.K, (uint64_t)s, (uint64_t)p.K * 2, 128, k.chunks) &&
               encode_3d_chunks(&k.tmA3, p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2,
                                (uint32_t)k.a_bytes / 128, k.chunks);
+    for (int l = 0; l < 3 && k.use3d; ++l)
+        k.use3d = encode_3d_chunks(&k.tmA3s[l], p.A, (uint64_t)p.K, (uint64_t)L * cR, (uint64_t)p.K * 2, 16u << l,
+                                   k.chunks);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);

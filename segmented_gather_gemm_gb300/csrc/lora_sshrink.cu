@@ -72,6 +72,19 @@ __device__ __forceinline__ ShWalk sh_walk(int ntiles, int nkc, int max_parts, in
     return wk;
 }
 
+// A box of a whole stage (3-D view): the smallest of 16, 32 or 64 rows that
+// covers the slot's 16 * n16 rows when that is below the full round16(c*R)
+// rows (tmA3s[level]), else the full box (level -1).  The chunks of the stage
+// then sit `a_stride` bytes apart.  Producer and MMA issuer both use it.
+__device__ __forceinline__ int sh_a3_level(const ShrinkParams &k, int n16) {
+    const int rows = n16 <= 1 ? 16 : (n16 <= 2 ? 32 : (n16 <= 4 ? 64 : (1 << 30)));
+    if (rows >= k.a_bytes / 128) return -1;
+    return rows == 16 ? 0 : (rows == 32 ? 1 : 2);
+}
+__device__ __forceinline__ int sh_a_stride(const ShrinkParams &k, int level) {
+    return level < 0 ? k.a_bytes : (16 << level) * 128;
+}
+
 // ------------------------------------------------------------------------------------- producer
 __device__ void sh_producer(const ShrinkParams &k, unsigned char *smem, const int *tables, int nruns, const ShWalk &wk,
                             int64_t nunits) {
@@ -126,7 +139,9 @@ __device__ void sh_producer(const ShrinkParams &k, unsigned char *smem, const in
             // round16(c*R) rows (rows past the rank feed no output column)
             const bool full3 = k.use3d && nch == k.chunks;
             const bool x3 = full3 && contig && xb < 0;
-            const uint32_t sbytes = (uint32_t)nch * (xbytes + (full3 ? (uint32_t)k.a_bytes : (uint32_t)n16 * 16 * 128));
+            const int alev = sh_a3_level(k, n16);
+            const uint32_t sbytes =
+                (uint32_t)nch * (xbytes + (full3 ? (uint32_t)sh_a_stride(k, alev) : (uint32_t)n16 * 16 * 128));
             mbar_wait(&W.empty[s], ((it / k.S) & 1) ^ 1, p.status, kStatusTimeout);
             unsigned char *st = smem + k.o_ring + s * k.stage_bytes;
             if (lane == 0) {
@@ -137,7 +152,7 @@ __device__ void sh_producer(const ShrinkParams &k, unsigned char *smem, const in
                     for (int j = 0; j < nch; ++j) tma_load_2d(st + j * 128 * 128, xmap, (ci + j) * 64, t0, &W.full[s]);
                 }
                 if (full3) {
-                    tma_load_3d(st + k.a_off, &k.tmA3, 0, T.w * cR, ci, &W.full[s]);
+                    tma_load_3d(st + k.a_off, alev < 0 ? &k.tmA3 : &k.tmA3s[alev], 0, T.w * cR, ci, &W.full[s]);
                 } else {
                     // A rows [0, 16 * n16) of each chunk as boxes of 64, then 32, then 16 rows
                     for (int j = 0; j < nch; ++j)
@@ -187,9 +202,13 @@ __device__ void sh_mma(const ShrinkParams &k, unsigned char *smem, const int *ta
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t sa = smem_u32(smem + k.o_ring + s * k.stage_bytes);
+                // A chunks as the producer laid them out: 3-D boxes of the
+                // stage's level, else one tile of a_bytes per chunk
+                const int astride = k.use3d && nch == k.chunks ? sh_a_stride(k, sh_a3_level(k, (p.c * r + 15) / 16))
+                                                               : k.a_bytes;
                 for (int j = 0; j < nch; ++j) {
                     const uint32_t xa = sa + j * 128 * 128;
-                    const uint32_t aa = sa + k.a_off + j * k.a_bytes;
+                    const uint32_t aa = sa + k.a_off + j * astride;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         tc_mma_bf16(d, smem_desc_kmajor(xa + ks * 32, 128), smem_desc_kmajor(aa + ks * 32, 128), idesc,

@@ -145,6 +145,7 @@ struct ShrinkParams {
     // rows, written [chunk][row][128 B] like the per-chunk tiles (use3d: K is
     // a multiple of 64 and both maps encoded)
     CUtensorMap tmX3, tmA3;
+    CUtensorMap tmA3s[3];  // the A view with boxes of 16, 32 and 64 rows (a slot whose c*r needs fewer rows)
     int use3d;
     LoraParams p;
     int runcap, max_segments;
