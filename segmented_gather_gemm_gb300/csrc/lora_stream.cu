@@ -4,6 +4,9 @@
 namespace csgmv {
 
 constexpr int kOpLoCol = kStOpCols / 2;  // the lo half of an operand buffer
+// stage pairs (st_mma): an even stage's B slot and accumulator have their
+// neighbours next to them, and two stages fit one MMA of N = 128
+static_assert(kStBSlots % 2 == 0 && kStAcc % 2 == 0 && kStCols == 64, "stage pairs");
 constexpr int kStOpBar = 1;              // named barrier of the operand warps
 
 struct StBars {
@@ -211,29 +214,37 @@ __device__ void st_mma(const StreamParams &k, unsigned char *smem, const int *ta
         const int RK = (r + 15) & ~15;
         const int ksteps = RK / 16;
         const uint32_t ahi = tmem + (uint32_t)(kStOpCol0 + b * kStOpCols), alo = ahi + kOpLoCol;
-        for (int i = 0; i < U.nt; ++i, ++g) {
+        // Stages go to the tensor core in pairs where they can: stage g (even)
+        // and g + 1 sit in neighbouring B slots and TMEM accumulators, so one
+        // MMA of N = 128 does both (half the MMA instructions, whose issue
+        // sets this warp's pace).
+        for (int i = 0; i < U.nt;) {
+            const int n = (g & 1) == 0 && i + 1 < U.nt ? 2 : 1;
             const int sb = g % k.Sb;
             const int a = g % kStAcc;
             // landed, padding columns [r, RK) zeroed by the B producer
-            mbar_wait(&W.b_ready[sb], (g / k.Sb) & 1, p.status, kStatusTimeout);
-            unsigned char *bs = smem + k.o_bring + sb * k.b_slot_bytes;
-            mbar_wait(&W.acc_empty[a], ((g / kStAcc) & 1) ^ 1, p.status, kStatusTimeout);
+            for (int j = 0; j < n; ++j)
+                mbar_wait(&W.b_ready[(g + j) % k.Sb], ((g + j) / k.Sb) & 1, p.status, kStatusTimeout);
+            for (int j = 0; j < n; ++j)
+                mbar_wait(&W.acc_empty[(g + j) % kStAcc], (((g + j) / kStAcc) & 1) ^ 1, p.status, kStatusTimeout);
             tc_fence_after();
             if (lane == 0) {
                 const int x0 = U.n0 + i * kStCols;
-                const int ncols = min(U.n1, x0 + kStCols) - x0;
+                const int ncols = min(U.n1, x0 + n * kStCols) - x0;
                 const uint32_t idesc = idesc_bf16_f32(128, (ncols + 15) & ~15);
-                const uint32_t bsa = smem_u32(bs);
+                const uint32_t bsa = smem_u32(smem + k.o_bring + sb * k.b_slot_bytes);
                 const uint32_t d = tmem + (uint32_t)(a * kStCols);
                 for (int ks = 0; ks < ksteps; ++ks) {
                     const uint64_t bd = smem_desc_kmajor(bsa + ks * 32, Rb);
                     tc_mma_bf16_tmem_a(d, ahi + ks * 8, bd, idesc, ks > 0);
                     tc_mma_bf16_tmem_a(d, alo + ks * 8, bd, idesc, true);
                 }
-                tc_commit(&W.b_empty[sb]);
-                tc_commit(&W.acc_full[a]);
+                for (int j = 0; j < n; ++j) tc_commit(&W.b_empty[(g + j) % k.Sb]);
+                for (int j = 0; j < n; ++j) tc_commit(&W.acc_full[(g + j) % kStAcc]);
             }
             __syncwarp();
+            i += n;
+            g += n;
         }
         ++uc;
     }
